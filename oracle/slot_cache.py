@@ -1,0 +1,172 @@
+"""Per-layer expert slot pool with LRU bookkeeping (oracle).
+
+Test infrastructure: see the package docstring.
+
+What it follows
+---------------
+* LRU kept as an ``OrderedDict`` with the front as least recently used: a hit
+  moves the expert to the end; a miss takes a free slot with ``list.pop()``
+  from ``list(range(capacity))`` (so the highest free index first), or else
+  evicts the front with ``popitem(last=False)``; the id->slot mapping is
+  updated in place and ``topk_ids`` are remapped through it
+  (vLLM PR #37190 "Run MoE models exceeding VRAM via expert CPU offloading with
+  GPU cache", sections "Architecture" and "How it works", and the review thread
+  that replaced the list with an OrderedDict).
+* The distinct experts of a step come from ``topk_ids.unique()``, i.e. in
+  ascending id order (same page, "How it works").
+* Bypass: a ubatch that touches more distinct experts than the pool has slots
+  does not go through the pool and takes the selective-copy path; nothing is
+  evicted (llama.cpp discussion #28248 "RFC: Persistent expert slot pool for
+  MoE CPU offload", section "Why not the other approaches on the table" and
+  "Design" item 2).  Rule used here: bypass iff (distinct non-cold experts) > N.
+* Cold set: chosen experts stay in pinned host memory, are read through UVA
+  and never enter the pool ("Running 125B MoE on Two 32 GB Cards", sections
+  2 and 3 "Only the least used experts in host RAM (offload-02)").
+
+Readings where the pages are open
+---------------------------------
+* Within a step, hits are touched first (ascending id), then misses are
+  filled (ascending id).  Because the non-cold distinct count D is at most N on
+  the pool path, the LRU front during the miss pass is never an expert used in
+  this step.
+* A bypass copies all D non-cold experts (resident ones too) into scratch at
+  index = rank of the expert among them; LRU state and hit/miss counters are
+  untouched.
+* An empty step (no ids) is not a step: nothing changes and nothing is counted.
+
+Slot-id encoding (the library's documented output encoding)
+-----------------------------------------------------------
+``kind << 29 | index`` with kind 0 = pool slot, 1 = bypass scratch position,
+2 = cold expert id (read from host memory).
+"""
+
+from __future__ import annotations
+
+from collections import OrderedDict
+from dataclasses import dataclass, field
+
+import numpy as np
+
+SLOT_KIND_SHIFT = 29
+SLOT_POOL = 0 << SLOT_KIND_SHIFT
+SLOT_SCRATCH = 1 << SLOT_KIND_SHIFT
+SLOT_COLD = 2 << SLOT_KIND_SHIFT
+
+
+def decode_slot_id(v: int) -> tuple[str, int]:
+    kind = v >> SLOT_KIND_SHIFT
+    idx = v & ((1 << SLOT_KIND_SHIFT) - 1)
+    return ({0: "pool", 1: "scratch", 2: "cold"}[kind], idx)
+
+
+@dataclass
+class PrepareRecord:
+    distinct: list = field(default_factory=list)   # ascending distinct ids
+    cold: list = field(default_factory=list)       # ascending cold ids
+    noncold: list = field(default_factory=list)    # ascending non-cold ids (D)
+    bypass: bool = False
+    hits: list = field(default_factory=list)       # ascending
+    misses: list = field(default_factory=list)     # (expert, slot, evicted|-1), ascending expert
+    copies: list = field(default_factory=list)     # (expert, dest index) in copy order
+    slot_ids: np.ndarray = None                    # int32, same shape as topk_ids
+
+
+STAT_KEYS = ("steps", "hits", "misses", "evictions", "bypass_steps", "cold_reads",
+             "bytes_h2d_miss", "bytes_h2d_bypass", "bytes_uva_cold")
+
+
+class LayerSlotCache:
+    """One MoE layer's pool of ``slots`` expert slots."""
+
+    def __init__(self, num_experts: int, slots: int, expert_bytes: int = 0, cold_mask=None):
+        if not 0 <= slots <= num_experts:
+            raise ValueError("need 0 <= slots <= num_experts")
+        self.E = num_experts
+        self.N = slots
+        self.B = expert_bytes
+        self.cold = (np.zeros(num_experts, dtype=bool) if cold_mask is None
+                     else np.asarray(cold_mask, dtype=bool).copy())
+        self.reset()
+
+    def reset(self):
+        self.lru: "OrderedDict[int, None]" = OrderedDict()   # front = least recently used
+        self.expert_to_slot: dict[int, int] = {}
+        self.free: list[int] = list(range(self.N))
+        self.stats = {k: 0 for k in STAT_KEYS}
+
+    # -- views used by tests -------------------------------------------------
+    def slot_map(self) -> np.ndarray:
+        m = np.full(self.E, -1, dtype=np.int32)
+        for e, s in self.expert_to_slot.items():
+            m[e] = s
+        return m
+
+    def slot_expert(self) -> np.ndarray:
+        m = np.full(self.N, -1, dtype=np.int32)
+        for e, s in self.expert_to_slot.items():
+            m[s] = e
+        return m
+
+    def lru_order(self) -> list:
+        return list(self.lru.keys())
+
+    # -- one step --------------------------------------------------------------
+    def prepare(self, topk_ids) -> PrepareRecord:
+        ids = np.asarray(topk_ids, dtype=np.int64)
+        rec = PrepareRecord()
+        if ids.size == 0:
+            rec.slot_ids = np.zeros(ids.shape, dtype=np.int32)
+            return rec
+        if ids.min() < 0 or ids.max() >= self.E:
+            raise ValueError("expert id out of range")
+        self.stats["steps"] += 1
+
+        rec.distinct = sorted(set(int(e) for e in ids.reshape(-1)))
+        rec.cold = [e for e in rec.distinct if self.cold[e]]
+        rec.noncold = [e for e in rec.distinct if not self.cold[e]]
+        self.stats["cold_reads"] += len(rec.cold)
+        self.stats["bytes_uva_cold"] += len(rec.cold) * self.B
+
+        scratch_pos = {}
+        if len(rec.noncold) > self.N:
+            rec.bypass = True
+            self.stats["bypass_steps"] += 1
+            self.stats["bytes_h2d_bypass"] += len(rec.noncold) * self.B
+            for r, e in enumerate(rec.noncold):
+                scratch_pos[e] = r
+                rec.copies.append((e, r))
+        else:
+            for e in rec.noncold:                      # hits first, ascending
+                if e in self.expert_to_slot:
+                    self.lru.move_to_end(e)
+                    rec.hits.append(e)
+                    self.stats["hits"] += 1
+            for e in rec.noncold:                      # then misses, ascending
+                if e in self.expert_to_slot:
+                    continue
+                evicted = -1
+                if self.free:
+                    s = self.free.pop()
+                else:
+                    evicted, _ = self.lru.popitem(last=False)
+                    s = self.expert_to_slot.pop(evicted)
+                    self.stats["evictions"] += 1
+                self.expert_to_slot[e] = s
+                self.lru[e] = None
+                rec.misses.append((e, s, evicted))
+                rec.copies.append((e, s))
+                self.stats["misses"] += 1
+                self.stats["bytes_h2d_miss"] += self.B
+
+        out = np.empty(ids.shape, dtype=np.int32)
+        flat_in, flat_out = ids.reshape(-1), out.reshape(-1)
+        for i, e in enumerate(flat_in):
+            e = int(e)
+            if self.cold[e]:
+                flat_out[i] = SLOT_COLD | e
+            elif rec.bypass:
+                flat_out[i] = SLOT_SCRATCH | scratch_pos[e]
+            else:
+                flat_out[i] = SLOT_POOL | self.expert_to_slot[e]
+        rec.slot_ids = out
+        return rec
