@@ -1,0 +1,398 @@
+"""Decode benchmark of the MoE layer through the GPU expert-slot cache.
+
+One step = one decode token through every MoE layer of the OLMoE-shaped
+workload (16 layers x 64 experts, top-8, H 2048, I 1024, bf16 weights, 16
+pool slots per layer): router top-k, slot bookkeeping + remap, host->device
+copies of missed experts, grouped expert MLP, residual add -- all in
+libmoecache.so kernels.  Inputs (routing logits and hidden states of every
+step) are resident in HBM before the timed region; every step reads 1.61 GB of
+expert weights, far more than the 129 MB L2, so no flush is needed.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line.  Under torchrun each rank runs an independent replica
+on its own GPU (the path has no exchange step); value = all tokens / the
+slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from expert_slot_cache_topk_gb300 import synth  # noqa: E402
+
+METRIC = "MoE decode tok/s with slot cache; miss H2D GB/s and GEMM HBM GB/s vs roof"
+UNIT = "tok/s"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def aggregate(seconds: float, units: float, world: int, device=None):
+    """(max seconds over ranks, sum of units over ranks); identity at world 1."""
+    if world <= 1:
+        return seconds, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.proc, self.lines = gpu, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+def workload_desc(w) -> str:
+    return (f"{w.name}-shaped decode: {w.layers} MoE layers x {w.experts} experts, top-{w.top_k}, "
+            f"hidden {w.hidden}, expert inter {w.inter}, {w.wdtype} weights, {w.slots} slots/layer, "
+            f"batch {w.tokens}, routing {w.routing} Zipf({w.zipf_s})"
+            + (f" with p={w.reuse_p} reuse" if w.reuse_p else ""))
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline / reference arm) -- the one place bench runs it
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """The CPU oracle (router top-k, OrderedDict slot pool, float64 dequant +
+    expert MLP, residual add) on a bounded sample of the decode workload:
+    `tokens` decode tokens through every layer, one (token, layer) step per
+    call.  Input generation happens here, outside any timed region."""
+
+    def __init__(self, w, tokens: int = 2):
+        from oracle import LayerSlotCache, expert_nbytes, router_topk
+        self.w = w
+        self.tokens = tokens
+        Be = expert_nbytes(w.wdtype, w.hidden, w.inter)["total"]
+        self.caches = [LayerSlotCache(w.experts, w.slots, Be) for _ in range(w.layers)]
+        self.lgs = [synth.routing_logits(w, l, tokens) for l in range(w.layers)]
+        x0 = synth.hidden_states(w, 0, tokens)
+        self.x0 = (x0.astype(np.float64) if w.wdtype == "f32"
+                   else (x0.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+        self.blocks = {}
+        for l in range(w.layers):
+            for s in range(tokens):
+                for e in np.unique(router_topk(self.lgs[l][s], w.top_k)[0]):
+                    if (l, int(e)) not in self.blocks:
+                        self.blocks[(l, int(e))] = synth.expert_block(w, l, int(e))
+        self.i = 0
+        self.x = None
+
+    def layer_step(self) -> float:
+        """Run the next (token, layer) step; returns its seconds."""
+        from oracle import dequant_expert, moe_combine, router_topk
+        w = self.w
+        n = self.tokens * w.layers
+        s, l = divmod(self.i % n, w.layers)
+        if l == 0:
+            self.x = self.x0[s].copy()
+        t0 = time.perf_counter()
+        ids, wts = router_topk(self.lgs[l][s], w.top_k)
+        self.caches[l].prepare(ids)
+        self.x = self.x + moe_combine(
+            self.x, ids, wts, lambda e: dequant_expert(self.blocks[(l, e)], w.wdtype, w.hidden, w.inter))
+        dt = time.perf_counter() - t0
+        self.i += 1
+        return dt
+
+
+def oracle_tokens_per_s(w, tokens: int = 2, budget_s: float = 20.0):
+    """Oracle decode throughput on a bounded sample: (tok/s, layer steps, seconds)."""
+    o = OracleSample(w, tokens)
+    o.layer_step()                      # first call pays numpy/BLAS start-up; not counted
+    o.i = 0
+    o.caches = [type(cc)(cc.E, cc.N, cc.B, cc.cold) for cc in o.caches]
+    done, spent = 0, 0.0
+    while done < tokens * w.layers and spent < budget_s:
+        spent += o.layer_step()
+        done += 1
+    return (done / w.layers) * w.tokens / spent, done, spent
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        if rank != 0:
+            dist.barrier()
+            return
+    o = OracleSample(w, tokens=2)
+    for _ in range(args.warmup):
+        o.layer_step()
+    total_s = sum(o.layer_step() for _ in range(args.steps))
+    tokens = args.steps / w.layers * w.tokens
+    value = tokens / total_s
+    sample = (f"each step = one (token, layer) step of the decode workload, cycling over 2 tokens "
+              f"x {w.layers} layers; value = (steps / {w.layers}) tokens / time")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded Zipf routing with reuse; N(0,0.02) weights)",
+        "config": {"workload": workload_desc(w)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+    from expert_slot_cache_topk_gb300 import _build
+    from expert_slot_cache_topk_gb300._abi import MOE_FWD_RESIDUAL, MoECache
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+
+    S = args.warmup + args.steps
+    c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, w.tokens,
+                 copy_mode=args.copy_mode, device=local_rank)
+    info = c.info()
+    t0 = time.time()
+    for l in range(w.layers):
+        synth.fill_layer_blocks(w, l, c.backing_view(l).reshape(-1), info["slot_stride"])
+    fill_s = time.time() - t0
+    lg = np.stack([synth.routing_logits(w, l, S) for l in range(w.layers)], axis=1)   # [S, L, T, E]
+    x0 = synth.hidden_states(w, 0, S)                                                 # [S, T, H]
+    lg_d = torch.from_numpy(lg).to(dev)
+    x0_d = torch.from_numpy(x0.view(np.int16)).to(dev).view(torch.bfloat16)
+    bufs = [torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(s):
+        x = x0_d[s]
+        for l in range(w.layers):
+            y = bufs[l & 1]
+            c.forward(l, x, lg_d[s, l], w.tokens, y, MOE_FWD_RESIDUAL, stream)
+            x = y
+        return x
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize(dev)
+    st0 = c.stats(-1)
+    launches0 = c.info()["kernel_launches"]
+    c.set_timing(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for s in range(args.warmup, S):
+            step(s)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    sec = ev0.elapsed_time(ev1) / 1e3
+    tm = c.read_timing()
+    c.set_timing(False)
+    st1 = c.stats(-1)
+    launches = c.info()["kernel_launches"] - launches0
+    tokens = args.steps * w.tokens
+    max_sec, all_tokens = aggregate(sec, tokens, world, dev)
+
+    # algorithmic bytes of the up (w13) kernel: k experts' w13 (+ scales) per launch
+    lay = synth.expert_layout(w.wdtype, w.hidden, w.inter)
+    up_bytes = w.tokens * w.top_k * (lay["w13"][1] + lay["s13"][1])     # batch 1: every expert read once
+    up_ms = tm["up_ms"] / max(tm["up_n"], 1)
+    pk = peaks()
+    achieved = up_bytes / (up_ms * 1e-3) / 1e9
+    miss_bytes = st1["bytes_h2d_miss"] - st0["bytes_h2d_miss"] + st1["bytes_h2d_bypass"] - st0["bytes_h2d_bypass"]
+    copy_s = tm["copy_ms"] / 1e3
+    h2d_peak = max(info["memcpy_gbs"], info["uva_gbs"]) if args.copy_mode == "auto" else None
+
+    # end-to-end through the C ABI with host buffers (copies inside the timed region)
+    e2e_steps = min(args.e2e_steps, S)
+    x_h = torch.from_numpy(x0.view(np.int16).copy()).pin_memory().numpy()
+    lg_h = torch.from_numpy(np.ascontiguousarray(lg)).pin_memory().numpy()
+    y_h = torch.empty((w.tokens, w.hidden), dtype=torch.int16).pin_memory().numpy()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for s in range(e2e_steps):
+        c.model_step_host(x_h[s], lg_h[s], w.tokens, y_h, 60000, stream)
+    e2e_s = time.perf_counter() - t0
+    e2e_sec, e2e_tok = aggregate(e2e_s, e2e_steps * w.tokens, world, dev)
+
+    line = None
+    if rank == 0:
+        cpu_v, cpu_n, cpu_dt = (None, 0, 0.0)
+        if world == 1 and not args.no_cpu_baseline:
+            cpu_v, cpu_n, cpu_dt = oracle_tokens_per_s(w, 2, budget_s=args.cpu_budget)
+        line = {
+            "metric": METRIC, "value": all_tokens / max_sec, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * max_sec / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded Zipf routing with reuse; N(0,0.02) weights)",
+            "config": {"workload": workload_desc(w), "tokens_per_step": w.tokens,
+                       "copy_mode": info["copy_mode_name"], "graph": False,
+                       "l2": "inputs larger than L2: every step reads "
+                             f"{w.layers * w.top_k * lay['total'] / 1e9:.2f} GB of expert weights",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "k_up (w13 + SiLU-mul)", "achieved": achieved,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                         "traffic": None, "peak_source": pk["source"],
+                         "bytes_per_launch": up_bytes, "avg_launch_us": up_ms * 1e3,
+                         "launches": tm["up_n"]},
+            "h2d": {"miss_bytes": miss_bytes, "copy_ms_total": tm["copy_ms"],
+                    "miss_gbs": (miss_bytes / copy_s / 1e9) if copy_s > 0 else None,
+                    "peak_gbs": h2d_peak, "memcpy_gbs_at_create": info["memcpy_gbs"],
+                    "uva_gbs_at_create": info["uva_gbs"]},
+            "phases_ms_per_step": {k[:-3]: tm[k] / args.steps for k in ("route_ms", "copy_ms", "up_ms", "down_ms")},
+            "cache": {k: st1[k] - st0[k] for k in ("hits", "misses", "evictions", "bypass_steps")},
+            "e2e": {"value": e2e_tok / e2e_sec, "unit": UNIT,
+                    "h2d_bytes_per_step": int(x_h[0].nbytes + lg_h[0].nbytes),
+                    "d2h_bytes_per_step": int(y_h.nbytes)},
+            "gpu_launches": int(launches),
+            "clocks": clk.summary(),
+            "setup_s": {"fill_weights": fill_s},
+        }
+        if cpu_v is not None:
+            line["cpu_baseline"] = {"value": cpu_v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                                    "sample": f"{cpu_n} (token, layer) steps of the first 2 decode tokens "
+                                              f"in {cpu_dt:.1f} s (float64 numpy, BLAS threads as installed)"}
+        print(json.dumps(line), flush=True)
+    c.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=480)
+    ap.add_argument("--warmup", type=int, default=32)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="olmoe", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--copy-mode", default="auto", choices=["auto", "uva", "memcpy"])
+    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

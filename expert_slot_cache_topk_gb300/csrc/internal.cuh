@@ -1,0 +1,106 @@
+// Internal declarations shared by the libmoecache translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_cache.h"
+
+namespace moe {
+
+constexpr int kPrepThreads = 1024;   // one CTA does the whole per-layer bookkeeping
+constexpr int kMlpThreads = 256;     // 8 warps per CTA in the expert MLP kernels
+constexpr int kCopyThreads = 256;
+constexpr int kCopyVecPerThread = 8; // 8 x 16 B in flight per thread
+constexpr int kCopyChunkVec = kCopyThreads * kCopyVecPerThread;  // 32 KiB per CTA step
+
+// Per-layer counters and LRU clock, device resident.
+enum {
+  ST_STEPS = 0, ST_HITS, ST_MISSES, ST_EVICT, ST_BYPASS, ST_COLD,
+  ST_B_MISS, ST_B_BYPASS, ST_B_COLD, ST_COUNT
+};
+
+struct LayerState {
+  unsigned long long clock;   // next recency stamp
+  int nfree;                  // free slots are exactly [0, nfree)
+  int pad;
+  unsigned long long stats[ST_COUNT];
+};
+
+// Header of the last prepare of a layer; the lists follow in a separate
+// [LST_COUNT][E] int32 block per layer.
+struct RecHdr {
+  int n_ids, bypass, n_distinct, n_cold, n_noncold, n_hits, n_misses, n_evictions;
+};
+enum { LST_HITS = 0, LST_MISS_E, LST_MISS_SLOT, LST_MISS_EV, LST_COLD, LST_NONCOLD, LST_COUNT };
+
+// Device error flag values (sticky until reset)
+enum { DEVERR_NONE = 0, DEVERR_BAD_ID = 1 };
+
+struct PrepArgs {
+  // fused router (do_route != 0): logits [T, E] -> ids / w
+  const float* logits;
+  float* w_out;
+  int do_route;
+  int renorm;
+  // ids [T*k] (read; written first when do_route)
+  int32_t* ids;
+  int T, k, E, N;
+  const uint8_t* cold;               // [E] of this layer, may be null
+  int32_t* slot_map;                 // [E]
+  int32_t* slot_expert;              // [N]
+  long long* slot_stamp;             // [N]
+  LayerState* st;
+  RecHdr* hdr;
+  int32_t* lists;                    // [LST_COUNT * E]
+  int32_t* slot_ids_out;             // [T*k] or null
+  unsigned long long* asg_ptr;       // [T*k] or null: expert block pointer per assignment
+  unsigned long long pool_base;      // this layer's pool
+  unsigned long long scratch_base;   // bypass scratch
+  unsigned long long host_base;      // device-usable address of this layer's backing store
+  unsigned long long stride;         // bytes between experts / slots
+  unsigned long long expert_bytes;
+  int* err;
+};
+
+struct CopyArgs {
+  const RecHdr* hdr;
+  const int32_t* lists;
+  int E;
+  const uint8_t* host_base;          // this layer's backing store (device-usable)
+  uint8_t* pool_base;                // this layer's pool
+  uint8_t* scratch_base;
+  unsigned long long stride;
+  unsigned long long nvec;           // 16-byte vectors per expert
+};
+
+struct MlpArgs {
+  const void* x;                     // [T, H] bf16 or f32
+  const unsigned long long* asg_ptr; // [T*k] expert block pointers (0 = skip)
+  const float* w;                    // [T*k]
+  float* h;                          // [T*k, I] scratch
+  void* y;                           // [T, H]
+  int T, k, H, I;
+  int residual;
+  unsigned long long off_w2, off_s13, off_s2;
+};
+
+// ---- launchers (k_route_prepare.cu) ----
+cudaError_t launch_router(const float* logits, int T, int E, int k, int renorm,
+                          int32_t* ids, float* w, cudaStream_t s);
+cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_copy(const CopyArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_copy_raw(const void* src, void* dst, unsigned long long nvec, int grid,
+                            cudaStream_t s);
+cudaError_t launch_verify(const int32_t* slot_expert, int N, const uint8_t* pool_base,
+                          const uint8_t* host_base, unsigned long long stride,
+                          unsigned long long nvec, int* mismatches, cudaStream_t s);
+
+// ---- launchers (k_mlp.cu) ----
+cudaError_t mlp_configure(int wdtype, int H, int I, int k);  // smem opt-in, call outside capture
+cudaError_t launch_mlp_up(int wdtype, const MlpArgs& a, cudaStream_t s);
+cudaError_t launch_mlp_down(int wdtype, const MlpArgs& a, cudaStream_t s);
+size_t mlp_down_smem_bytes(int k, int I);
+size_t mlp_up_smem_bytes(int H);
+
+}  // namespace moe

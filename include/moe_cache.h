@@ -1,0 +1,303 @@
+/*
+ * moe_cache.h -- C ABI of libmoecache.so
+ *
+ * One MoE layer forward through a persistent per-layer GPU expert-slot cache,
+ * on one NVIDIA GB300 (sm_103a).  Routed expert weights live in a pinned host
+ * backing store owned by the library; each layer has a fixed-address pool of
+ * N expert slots in HBM.  A step runs router top-k, the LRU hit/miss/evict
+ * bookkeeping with the id->slot remap, the host-to-device copy of missed
+ * experts into their victim slots, and the grouped expert MLP (gate/up w13,
+ * SiLU-mul, down w2, top-k weighted combine) indexed by slot.
+ *
+ * Sources (web pages this library restates; cited by title and section):
+ *  [vLLM #37190]  "[MoE][Offload] Run MoE models exceeding VRAM via expert CPU
+ *                 offloading with GPU cache (--moe-expert-cache-size)"
+ *  [llama.cpp #28248] "RFC: Persistent expert slot pool for MoE CPU offload
+ *                 (--moe-expert-cache)"
+ *  [Flash-Next 2x32GB] "Running 125B MoE on Two 32 GB Cards - vLLM
+ *                 Optimization Edition"
+ *  [vLLM #51710 article] czykbl.com article on vLLM PR #51710 (layer prefetch)
+ *
+ * Conventions for every entry point
+ *  - Return a moe_status; on failure moe_cache_last_error() holds a message.
+ *    Invalid arguments are rejected before any GPU work (MOE_EINVAL).
+ *  - Pointers suffixed _d are device pointers (or pointers the device can
+ *    dereference), _h are host pointers.  The caller owns every buffer it
+ *    passes; the library owns the backing store, pools, scratch, device
+ *    state, its copy stream and its events.
+ *  - Work is stream-ordered on the caller's stream (a cudaStream_t passed as
+ *    void*; NULL = legacy default stream).  Work the library issues on its
+ *    internal copy stream is joined back to the caller's stream before the
+ *    call returns, so later work on that stream sees the filled slots.
+ *  - A handle is single-threaded and single-stream: calls on one handle must
+ *    not overlap (the pages make the same single-threaded assumption,
+ *    [vLLM #37190] review point 1 "Thread safety").
+ *  - Device-side input errors (an expert id outside [0, E) reaching prepare)
+ *    do not fault: that whole step is skipped (pool state untouched, slot ids
+ *    written as -1, every assignment contributes zero to y), a sticky device
+ *    error flag is set, and the next synchronising call (moe_cache_check,
+ *    moe_cache_stats, moe_cache_last_prepare, moe_cache_get_state) returns
+ *    MOE_ESTATE.  moe_cache_reset clears it.
+ */
+#ifndef MOE_CACHE_H
+#define MOE_CACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_cache moe_cache_t;   /* opaque, library-owned */
+typedef void* moe_stream_t;             /* cudaStream_t */
+
+/* Weight formats.  Canonical expert block layout, every part row-major:
+ *   [ w13 [2I, H] | w2 [H, I] | s13 [2I, H/128] | s2 [H, I/128] ]
+ * w13 rows [0, I) are the gate projection, rows [I, 2I) the up projection.
+ *  MOE_F32       f32 weights, no scales.
+ *  MOE_BF16      bf16 weights, no scales.
+ *  MOE_INT4_G128 two 4-bit codes per byte along the row, low nibble = even
+ *                column; weight = (code - 8) * scale, one bf16 scale per 128
+ *                consecutive columns of a row; no zero point.  H and I must be
+ *                multiples of 128.  At w13 [1280, 2560] + w2 [2560, 640] this
+ *                is 2,534,400 bytes = 2.417 MiB ([Flash-Next 2x32GB] section 1
+ *                "What does not fit").
+ * Hidden states x / y are f32 for MOE_F32 and bf16 otherwise. */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_INT4_G128 = 2 } moe_wdtype;
+
+/* How missed experts reach their slot.
+ *  MOE_COPY_MEMCPY  prepare reads the miss list back to the host (one small
+ *                   read-back per layer step, as in [llama.cpp #28248]
+ *                   "Design" item 3) and issues one cudaMemcpyAsync per miss
+ *                   on the copy stream.  Not capturable in a CUDA graph.
+ *  MOE_COPY_UVA     an SM copy kernel on the copy stream reads the device-side
+ *                   miss list and copies from the mapped pinned host store with
+ *                   16-byte loads.  No host round trip; graph-capturable.
+ *  MOE_COPY_AUTO    at create, time both on the backing store and keep the
+ *                   faster (moe_cache_info reports the two bandwidths). */
+typedef enum { MOE_COPY_AUTO = 0, MOE_COPY_MEMCPY = 1, MOE_COPY_UVA = 2 } moe_copy_mode;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,    /* bad argument, nothing done */
+  MOE_ENOMEM = -2,    /* host/device allocation failed or over the HBM budget */
+  MOE_ECUDA = -3,     /* a CUDA call failed; message holds cudaGetErrorString */
+  MOE_ETIMEOUT = -4,  /* a bounded host wait on the GPU gave up */
+  MOE_ESTATE = -5     /* call not valid in the current state, or device error flag set */
+} moe_status;
+
+/* Slot-id encoding written by prepare (one per routed id):
+ *   kind << 29 | index
+ *   MOE_SLOT_POOL    index = pool slot in [0, N)
+ *   MOE_SLOT_SCRATCH index = bypass scratch position = rank of the expert among
+ *                    the step's distinct non-cold experts (ascending id)
+ *   MOE_SLOT_COLD    index = expert id; read in place from pinned host memory */
+#define MOE_SLOT_KIND_SHIFT 29
+#define MOE_SLOT_POOL (0u << MOE_SLOT_KIND_SHIFT)
+#define MOE_SLOT_SCRATCH (1u << MOE_SLOT_KIND_SHIFT)
+#define MOE_SLOT_COLD (2u << MOE_SLOT_KIND_SHIFT)
+#define MOE_SLOT_INDEX_MASK ((1u << MOE_SLOT_KIND_SHIFT) - 1u)
+
+/* moe_forward flags */
+#define MOE_FWD_RESIDUAL 1   /* y = x + MoE(x) instead of y = MoE(x) */
+
+/* Limits checked at create */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 32
+
+typedef struct {
+  int num_layers;        /* L >= 1 */
+  int num_experts;       /* E, 1..MOE_MAX_EXPERTS */
+  int top_k;             /* k, 1..min(E, MOE_MAX_TOPK) */
+  int hidden;            /* H */
+  int inter;             /* I, expert intermediate size */
+  int wdtype;            /* moe_wdtype */
+  int slots_per_layer;   /* N, 0..E; 0 = every step bypasses the pool */
+  int max_tokens;        /* largest T per call; sizes scratch and id buffers */
+  int renormalize;       /* 0: weights = softmax probs of the chosen; 1: divided by their sum */
+  const uint8_t* cold_mask_h; /* [L*E] nonzero = cold (never pooled, read via UVA); NULL = none. Copied. */
+  int copy_mode;         /* moe_copy_mode */
+  int device;            /* CUDA device ordinal */
+  size_t hbm_budget_bytes; /* cap on pool + scratch bytes; 0 = half of free device memory */
+} moe_cache_config;
+
+/* Cumulative per-layer counters (moe_cache_stats with layer = -1 sums layers).
+ * hits/misses count once per distinct expert per pool-path step
+ * ([vLLM #37190] "How it works"); bypass steps count neither. */
+typedef struct {
+  uint64_t steps;            /* prepare calls with T > 0 */
+  uint64_t hits;
+  uint64_t misses;
+  uint64_t evictions;
+  uint64_t bypass_steps;     /* steps with distinct non-cold experts > N */
+  uint64_t cold_reads;       /* distinct cold experts read in place */
+  uint64_t bytes_h2d_miss;   /* misses * expert bytes */
+  uint64_t bytes_h2d_bypass; /* sum over bypass steps of D * expert bytes */
+  uint64_t bytes_uva_cold;   /* cold_reads * expert bytes */
+} moe_cache_counters;
+
+/* Result of the last prepare of one layer (moe_cache_last_prepare).
+ * Array pointers are caller-owned host buffers of at least E entries each, or
+ * NULL to skip that list. */
+typedef struct {
+  int n_ids;         /* T*k of that step */
+  int bypass;        /* 1 if the step took the bypass path */
+  int n_distinct, n_cold, n_noncold;
+  int n_hits, n_misses, n_evictions;
+  int32_t* hits_h;           /* [n_hits] ascending */
+  int32_t* miss_expert_h;    /* [n_misses] ascending expert id */
+  int32_t* miss_slot_h;      /* [n_misses] slot it was copied into */
+  int32_t* miss_evicted_h;   /* [n_misses] expert evicted from that slot, -1 if free */
+  int32_t* cold_h;           /* [n_cold] ascending */
+  int32_t* noncold_h;        /* [n_noncold] ascending; on bypass, scratch position = index */
+} moe_prepare_info;
+
+typedef struct {
+  size_t expert_bytes;       /* B_e, canonical block size */
+  size_t slot_stride;        /* bytes between slots / backing experts (B_e rounded up to 256) */
+  size_t pool_bytes;         /* L*N*slot_stride in HBM */
+  size_t scratch_bytes;      /* bypass scratch in HBM */
+  size_t backing_bytes;      /* L*E*slot_stride pinned host */
+  int copy_mode;             /* the mode in use (AUTO resolved) */
+  double memcpy_gbs;         /* measured at create (AUTO only, else 0) */
+  double uva_gbs;            /* measured at create (AUTO only, else 0) */
+  uint64_t kernel_launches;  /* kernels launched by this handle so far */
+  int scratch_experts;       /* bypass scratch capacity in experts */
+} moe_cache_info;
+
+/* Per-phase GPU time accumulated while timing is on (CUDA events on the
+ * stream each kernel is launched on).  Works under stream capture too: the
+ * events become graph nodes and are read after the graph has run. */
+typedef struct {
+  double route_ms, copy_ms, up_ms, down_ms;   /* router+prepare, miss/bypass copy, w13, w2 */
+  uint64_t route_n, copy_n, up_n, down_n;     /* launches timed */
+} moe_cache_timing;
+
+/* ---------------------------------------------------------------- lifecycle */
+
+/* Allocate the pinned backing store (L*E experts), the per-layer pools
+ * (fixed addresses for the handle's life, [vLLM #37190] "torch.compile
+ * compatibility"), the bypass scratch (min(E, max_tokens*k) experts), device
+ * state (all slots free), the copy stream and events.  Fails with MOE_ENOMEM
+ * when pools + scratch exceed the budget (default: half of free device memory,
+ * [llama.cpp #28248] "Design" item 4) -- never a silent downgrade
+ * ([vLLM #37190] "Changes": errors instead of silent downgrades).
+ * On failure *out is NULL and moe_cache_last_error(NULL) has the reason. */
+moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out);
+
+/* Free everything.  NULL is ignored.  Synchronises the device first. */
+void moe_cache_destroy(moe_cache_t* c);
+
+/* Message of the last failure on c, or of the last failed create when c is NULL. */
+const char* moe_cache_last_error(const moe_cache_t* c);
+
+/* Bytes of one canonical expert block for a format and shape. */
+moe_status moe_cache_expert_bytes(int wdtype, int hidden, int inter, size_t* bytes);
+
+moe_status moe_cache_get_info(moe_cache_t* c, moe_cache_info* out);
+
+/* -------------------------------------------------------------- weights in */
+
+/* Host address (pinned, device-mapped) where expert (layer, expert)'s block
+ * lives, so a caller can write it in place; *stride_bytes = slot stride. */
+moe_status moe_cache_backing_ptr(moe_cache_t* c, int layer, int expert,
+                                 void** block_h, size_t* stride_bytes);
+
+/* Copy one canonical block (bytes must equal expert_bytes) into the backing
+ * store.  Host-synchronous.  If the expert currently sits in a pool slot the
+ * slot is refreshed too, so pool and backing never disagree. */
+moe_status moe_cache_load_expert(moe_cache_t* c, int layer, int expert,
+                                 const void* block_h, size_t bytes);
+
+/* ------------------------------------------------------------- hot path */
+
+/* Router top-k: logits_d f32 [T, E] -> ids_d int32 [T, k], w_d f32 [T, k].
+ * ids are the k largest logits in descending order, lower id first on equal
+ * logits ([Flash-Next 2x32GB] section 4.2, "the lower id wins"); NaN ranks
+ * below every number.  w = softmax over all E of the chosen (divided by their
+ * sum when renormalize).  One warp per token. */
+moe_status moe_cache_router(moe_cache_t* c, const float* logits_d, int T,
+                            int32_t* ids_d, float* w_d, moe_stream_t stream);
+
+/* Pool bookkeeping + remap + copies for one layer step.
+ * ids_d int32 [T, k] (device).  Distinct ids are taken in ascending order
+ * ([vLLM #37190] "How it works": topk_ids.unique()).  Cold experts are read
+ * in place.  If the distinct non-cold count D exceeds N the step bypasses the
+ * pool: all D experts are copied to scratch in ascending id order and the
+ * LRU state is untouched ([llama.cpp #28248] "Why not the other approaches on
+ * the table").  Otherwise hits are touched first (ascending), then each miss
+ * (ascending) takes the highest free slot or evicts the least recently used
+ * slot not used this step ([vLLM #37190] "Architecture", OrderedDict LRU), and
+ * is copied host-to-device into that slot.  slot_ids_d int32 [T, k] receives
+ * the encoded slot ids (NULL = don't write).  On return the copies are
+ * ordered before later work on `stream`. */
+moe_status moe_cache_prepare(moe_cache_t* c, int layer, const int32_t* ids_d, int T,
+                             int32_t* slot_ids_d, moe_stream_t stream);
+
+/* Read back the last prepare of `layer` (synchronises the device). */
+moe_status moe_cache_last_prepare(moe_cache_t* c, int layer, moe_prepare_info* out);
+
+/* The whole layer: router + prepare + copies + grouped expert MLP.
+ * x_d [T, H] and y_d [T, H] (bf16, or f32 for MOE_F32) are caller-owned and
+ * may not alias; logits_d f32 [T, E].  y[t] = sum_j w[t,j] * W2_e silu(Wg_e x)
+ * * (Wu_e x) summed in j order, with weights read from the slot / scratch /
+ * cold host copy of expert e ([vLLM #37190] "How it works": fused_experts on
+ * slot buffers with remapped ids).  flags: MOE_FWD_RESIDUAL adds x. */
+moe_status moe_forward(moe_cache_t* c, int layer, const void* x_d, const float* logits_d,
+                       int T, void* y_d, int flags, moe_stream_t stream);
+
+/* Grouped expert MLP alone, no cache: for each assignment a = t*k + j,
+ * block_ptrs_d[a] is a device-readable pointer to expert e's canonical block
+ * (HBM or mapped pinned host; 0 = skip, contributes zero) and w_d[a] its
+ * weight.  h_scratch_d is caller-provided scratch of T*k*I floats.  Same
+ * arithmetic and summation order as moe_forward. */
+moe_status moe_expert_mlp(int wdtype, int hidden, int inter, int top_k,
+                          const void* x_d, const uint64_t* block_ptrs_d, const float* w_d,
+                          int T, float* h_scratch_d, void* y_d, int flags,
+                          moe_stream_t stream);
+
+/* End-to-end step from host buffers: copies x_h [T, H] and logits_h
+ * [L, T, E] (pinned host recommended) to the device, runs every layer as
+ * x <- x + MoE_l(x), copies the final x back to y_h [T, H] and waits for it
+ * (bounded wait, MOE_ETIMEOUT after timeout_ms). */
+moe_status moe_model_step_host(moe_cache_t* c, const void* x_h, const float* logits_h, int T,
+                               void* y_h, int timeout_ms, moe_stream_t stream);
+
+/* ------------------------------------------------------------ inspection */
+
+/* Cumulative counters of one layer, or the sum over layers (layer = -1).
+ * Synchronises the device. */
+moe_status moe_cache_stats(moe_cache_t* c, int layer, moe_cache_counters* out);
+
+/* Device state of one layer (synchronises): slot_map_h int32[E] (-1 absent),
+ * slot_expert_h int32[N] (-1 free), slot_stamp_h int64[N] (recency stamp,
+ * larger = more recent).  Any pointer may be NULL.  *n_free_h (may be NULL)
+ * receives the free-slot count. */
+moe_status moe_cache_get_state(moe_cache_t* c, int layer, int32_t* slot_map_h,
+                               int32_t* slot_expert_h, int64_t* slot_stamp_h, int32_t* n_free_h);
+
+/* Compare every occupied slot of `layer` with its expert's backing block on
+ * the GPU; *mismatched_slots receives the number of slots whose bytes differ
+ * ([vLLM #37190] "Test results": test_gpu_buffer_matches_source_weights).
+ * Synchronises the device. */
+moe_status moe_cache_verify_slots(moe_cache_t* c, int layer, int* mismatched_slots);
+
+/* Device pointers of a layer's pool and of the bypass scratch. */
+moe_status moe_cache_pool_ptrs(moe_cache_t* c, int layer, void** pool_d, void** scratch_d);
+
+/* Synchronise and report the sticky device error flag (MOE_ESTATE if set). */
+moe_status moe_cache_check(moe_cache_t* c);
+
+/* Empty every pool, zero the counters and the device error flag. */
+moe_status moe_cache_reset(moe_cache_t* c);
+
+/* Per-phase event timing: on != 0 starts (and clears) accumulation. */
+moe_status moe_cache_set_timing(moe_cache_t* c, int on);
+/* Synchronises the device and returns the accumulated per-phase times. */
+moe_status moe_cache_read_timing(moe_cache_t* c, moe_cache_timing* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_CACHE_H */

@@ -1,0 +1,298 @@
+"""The whole layer on the GPU (router -> prepare -> copies -> grouped expert
+MLP) against the float64 oracle, plus the invariants the pages state:
+cached output == all-resident == bypass == cold (bitwise, same kernels),
+copy modes agree, slots hold their expert's bytes, graph capture replays,
+and bad input fails without faulting."""
+
+import numpy as np
+import pytest
+
+from expert_slot_cache_topk_gb300 import synth
+from expert_slot_cache_topk_gb300._abi import MoeError, MOE_EINVAL, MOE_ENOMEM, MOE_ESTATE, MOE_FWD_RESIDUAL
+from oracle import router_topk
+from tests.gpu_util import (OracleWeights, assert_close, empty_y, make_cache, oracle_slot_caches,
+                            oracle_y, torch_x, x_to_f64, y_to_f64)
+
+pytestmark = pytest.mark.gpu
+W = synth.WORKLOADS
+
+
+def _forward_steps(c, w, layer, xs, lgs, flags=0):
+    import torch
+    ys = []
+    for x, lg in zip(xs, lgs):
+        T = lg.shape[0]
+        y = empty_y(w, T)
+        c.forward(layer, torch_x(w, x), torch.from_numpy(lg).cuda(), T, y, flags)
+        ys.append(y)
+    torch.cuda.synchronize()
+    return ys
+
+
+@pytest.mark.parametrize("name,L,steps,slots", [
+    ("tiny", 1, 64, None),
+    ("olmoe", 2, 10, None),
+    ("int4", 2, 10, 16),
+    ("int4", 1, 6, 0),
+])
+def test_forward_matches_oracle(name, L, steps, slots):
+    w = W[name].with_(layers=L)
+    c = make_cache(w, slots=slots)
+    wt = OracleWeights(w)
+    for l in range(L):
+        lgs = synth.routing_logits(w, l, steps)
+        xs = synth.hidden_states(w, l, steps)
+        ys = _forward_steps(c, w, l, xs, lgs)
+        for s in range(steps):
+            ref = oracle_y(w, wt, l, xs[s], lgs[s])
+            assert_close(y_to_f64(w, ys[s]), ref, f"{name} layer {l} step {s}")
+    c.check()
+    c.close()
+
+
+def test_forward_batched_bypass_sampled_tokens():
+    w = W["batched"].with_(layers=1)
+    c = make_cache(w)
+    wt = OracleWeights(w)
+    lgs = synth.routing_logits(w, 0, 2)
+    xs = synth.hidden_states(w, 0, 2)
+    ys = _forward_steps(c, w, 0, xs, lgs)
+    assert c.stats(0)["bypass_steps"] == 2
+    g = np.random.default_rng(0)
+    for s in range(2):
+        toks = g.choice(w.tokens, 8, replace=False)
+        ref = oracle_y(w, wt, 0, xs[s][toks], lgs[s][toks])
+        assert_close(y_to_f64(w, ys[s])[toks], ref, f"batched step {s}")
+    c.close()
+
+
+def test_forward_prefill_with_cold_set_sampled_tokens():
+    w = W["prefill_cold"].with_(layers=1, prefill_tokens=512)
+    c = make_cache(w, max_tokens=512)
+    wt = OracleWeights(w)
+    lg = synth.prefill_logits(w, 0)
+    x = synth.hidden_states(w, 0, 1, tokens=512)[0]
+    (y,) = _forward_steps(c, w, 0, [x], [lg])
+    st = c.stats(0)
+    assert st["bypass_steps"] == 1 and st["misses"] == 0 and st["cold_reads"] > 0
+    sm, _, _, nfree = c.get_state(0)
+    assert (sm == -1).all() and nfree == w.slots          # prefill leaves the pool untouched
+    g = np.random.default_rng(1)
+    toks = g.choice(512, 24, replace=False)
+    ref = oracle_y(w, wt, 0, x[toks], lg[toks])
+    assert_close(y_to_f64(w, y)[toks], ref, "prefill")
+    # decode after prefill, cold experts read in place
+    lgs = synth.routing_logits(w, 0, 6)
+    xs = synth.hidden_states(w, 0, 6)
+    ys = _forward_steps(c, w, 0, xs, lgs)
+    for s in range(6):
+        assert_close(y_to_f64(w, ys[s]), oracle_y(w, wt, 0, xs[s], lgs[s]), f"decode {s}")
+    c.close()
+
+
+@pytest.mark.parametrize("name", ["olmoe", "int4"])
+def test_cached_resident_bypass_cold_bitwise_equal(name):
+    """Same kernel, different homes for the expert bytes -> identical y."""
+    import torch
+    w = W[name].with_(layers=1)
+    steps = 12
+    lgs = synth.routing_logits(w, 0, steps)
+    xs = synth.hidden_states(w, 0, steps)
+    outs = {}
+    variants = {
+        "cached": dict(slots=w.top_k + 2),
+        "resident": dict(slots=w.experts),
+        "bypass": dict(slots=0),
+        "cold": dict(slots=w.top_k, cold=np.ones((1, w.experts), np.uint8)),
+        "memcpy": dict(slots=w.top_k + 2, copy_mode="memcpy"),
+    }
+    for key, kw in variants.items():
+        c = make_cache(w, **kw)
+        outs[key] = [y.view(torch.int16).cpu().numpy() for y in _forward_steps(c, w, 0, xs, lgs)]
+        if key == "cold":
+            assert c.stats(0)["cold_reads"] > 0 and c.stats(0)["misses"] == 0
+        c.close()
+    for key in variants:
+        for s in range(steps):
+            assert (outs[key][s] == outs["cached"][s]).all(), (key, s)
+
+
+def test_slots_hold_their_experts_after_churn():
+    w = W["int4"].with_(layers=2, hidden=256, inter=128)
+    c = make_cache(w, slots=12)
+    for l in range(2):
+        _forward_steps(c, w, l, synth.hidden_states(w, l, 40), synth.routing_logits(w, l, 40))
+        assert c.verify_slots(l) == 0
+        st = c.stats(l)
+        assert st["evictions"] > 0
+    c.close()
+
+
+def test_load_expert_refreshes_a_resident_slot():
+    import torch
+    w = W["tiny"]
+    c = make_cache(w)
+    lgs = synth.routing_logits(w, 0, 3)
+    xs = synth.hidden_states(w, 0, 3)
+    _forward_steps(c, w, 0, xs[:1], lgs[:1])
+    ids, _ = router_topk(lgs[0], w.top_k)
+    e = int(ids[0, 0])
+    blk = synth.expert_block(w, 0, e).copy()
+    blk.view(np.float32)[:] *= 2.0
+    c.load_expert(0, e, blk)
+    assert c.verify_slots(0) == 0
+    (y,) = _forward_steps(c, w, 0, xs[:1], lgs[:1])
+    wt = OracleWeights(w)
+    from oracle import dequant_expert
+    wt.cache[(0, e)] = dequant_expert(blk, w.wdtype, w.hidden, w.inter)
+    assert_close(y_to_f64(w, y), oracle_y(w, wt, 0, xs[0], lgs[0]), "after reload")
+    c.close()
+
+
+def test_residual_flag_and_expert_mlp_entry_point():
+    import torch
+    from expert_slot_cache_topk_gb300._abi import expert_mlp
+    w = W["olmoe"].with_(layers=1)
+    c = make_cache(w)
+    lg = synth.routing_logits(w, 0, 1)[0]
+    x = synth.hidden_states(w, 0, 1)[0]
+    (y,) = _forward_steps(c, w, 0, [x], [lg])
+    (yr,) = _forward_steps(c, w, 0, [x], [lg], flags=MOE_FWD_RESIDUAL)
+    xt = torch_x(w, x)
+    ref = xt.float() + y.float()
+    assert ((yr.float() - ref).abs() <= 2e-2 + 1e-2 * ref.abs()).all()
+    # standalone grouped MLP on the same pool slots
+    ids, wts = router_topk(lg, w.top_k)
+    sm, _, _, _ = c.get_state(0)
+    pool, _ = c.pool_ptrs(0)
+    stride = c.info()["slot_stride"]
+    ptrs = torch.tensor([pool + int(sm[e]) * stride for e in ids[0]], dtype=torch.int64, device="cuda")
+    wd = torch.tensor(wts.astype(np.float32), device="cuda")
+    h = torch.empty((w.top_k, w.inter), dtype=torch.float32, device="cuda")
+    y2 = empty_y(w, 1)
+    expert_mlp("bf16", w.hidden, w.inter, w.top_k, xt, ptrs, wd, 1, h, y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y)          # same kernels, same bytes, same order
+    c.close()
+
+
+def test_graph_capture_uva_replays_like_eager():
+    import torch
+    w = W["olmoe"].with_(layers=2, hidden=512, inter=256)
+    steps = 6
+    lgs = [synth.routing_logits(w, l, steps) for l in range(2)]
+    xs = [synth.hidden_states(w, l, steps) for l in range(2)]
+    ref = make_cache(w, slots=10)
+    ref_y = [[y.clone() for y in _forward_steps(ref, w, l, xs[l], lgs[l])] for l in range(2)]
+    c = make_cache(w, slots=10)
+    x_st = [torch_x(w, xs[l][0]).clone() for l in range(2)]
+    lg_st = [torch.from_numpy(lgs[l][0]).cuda() for l in range(2)]
+    y_st = [empty_y(w, 1) for _ in range(2)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for l in range(2):
+                c.forward(l, x_st[l], lg_st[l], 1, y_st[l], 0, torch.cuda.current_stream())
+    torch.cuda.current_stream().wait_stream(s)
+    for st in range(steps):
+        for l in range(2):
+            x_st[l].copy_(torch_x(w, xs[l][st]))
+            lg_st[l].copy_(torch.from_numpy(lgs[l][st]).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        for l in range(2):
+            assert torch.equal(y_st[l], ref_y[l][st]), (st, l)
+    for l in range(2):
+        assert c.stats(l) == ref.stats(l)
+    ref.close()
+    c.close()
+
+
+def test_memcpy_mode_refuses_capture():
+    import torch
+    w = W["tiny"]
+    c = make_cache(w, copy_mode="memcpy")
+    x = torch_x(w, synth.hidden_states(w, 0, 1)[0])
+    lg = torch.from_numpy(synth.routing_logits(w, 0, 1)[0]).cuda()
+    y = empty_y(w, 1)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(Exception):
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                c.forward(0, x, lg, 1, y, 0, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    c.close()
+
+
+def test_model_step_host_matches_layer_chain():
+    import torch
+    w = W["olmoe"].with_(layers=3, hidden=512, inter=256)
+    a = make_cache(w)
+    b = make_cache(w)
+    x0 = synth.hidden_states(w, 0, 1)[0]
+    lg = np.stack([synth.routing_logits(w, l, 1)[0] for l in range(3)])
+    y_h = np.zeros_like(x0)
+    a.model_step_host(x0, lg, 1, y_h)
+    x = torch_x(w, x0)
+    for l in range(3):
+        y = empty_y(w, 1)
+        b.forward(l, x, torch.from_numpy(lg[l]).cuda(), 1, y, MOE_FWD_RESIDUAL)
+        x = y
+    torch.cuda.synchronize()
+    assert (x.view(torch.int16).cpu().numpy() == y_h.view(np.int16)).all()
+    a.close()
+    b.close()
+
+
+def test_counters_closed_forms():
+    w = W["int4"].with_(layers=1, hidden=256, inter=128)
+    c = make_cache(w, slots=16)
+    oc = oracle_slot_caches(w, slots=16)[0]
+    lgs = synth.routing_logits(w, 0, 30)
+    _forward_steps(c, w, 0, synth.hidden_states(w, 0, 30), lgs)
+    Be = c.info()["expert_bytes"]
+    s = c.stats(0)
+    D = 0
+    for lg in lgs:
+        ids, _ = router_topk(lg, w.top_k)
+        oc.prepare(ids)
+        D += len(set(ids.reshape(-1).tolist()))
+    assert s["hits"] + s["misses"] == D
+    assert s["bytes_h2d_miss"] == s["misses"] * Be == oc.stats["bytes_h2d_miss"]
+    assert s == oc.stats
+    c.close()
+
+
+def test_errors_do_not_fault():
+    import torch
+    from expert_slot_cache_topk_gb300._abi import MoECache
+    w = W["tiny"]
+    with pytest.raises(MoeError) as ei:
+        MoECache(1, 8, 2, 64, 128, "f32", 4, 1, hbm_budget_bytes=1000)
+    assert ei.value.status == MOE_ENOMEM
+    with pytest.raises(MoeError) as ei:
+        MoECache(1, 8, 9, 64, 128, "f32", 4, 1)
+    assert ei.value.status == MOE_EINVAL
+    c = make_cache(w)
+    lg = torch.from_numpy(synth.routing_logits(w, 0, 1)[0]).cuda()
+    x = torch_x(w, synth.hidden_states(w, 0, 1)[0])
+    y = empty_y(w, 2)
+    with pytest.raises(MoeError) as ei:
+        c.forward(0, x, lg, 2, y)                 # T > max_tokens
+    assert ei.value.status == MOE_EINVAL
+    with pytest.raises(MoeError):
+        c.forward(1, x, lg, 1, y)                 # no such layer
+    bad = torch.tensor([[3, 8]], dtype=torch.int32, device="cuda")
+    out = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    c.prepare(0, bad, 1, out)
+    with pytest.raises(MoeError) as ei:
+        c.check()
+    assert ei.value.status == MOE_ESTATE
+    assert (out.cpu() == -1).all()
+    c.reset()
+    c.check()
+    assert c.stats(0)["steps"] == 0
+    c.close()
