@@ -86,6 +86,7 @@ SIGNATURES = {
     "moe_cache_last_prepare": (_S, [_H, _I, C.POINTER(moe_prepare_info)]),
     "moe_forward": (_S, [_H, _I, _P, _P, _I, _P, _I, _P]),
     "moe_expert_mlp": (_S, [_I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _I, _P]),
+    "moe_expert_mlp_noalloc": (_S, [_I, _I, _I, _I, _P, _P, _P, _I, _P, _I, _P]),
     "moe_model_step_host": (_S, [_H, _P, _P, _I, _P, _I, _P]),
     "moe_cache_stats": (_S, [_H, _I, C.POINTER(moe_cache_counters)]),
     "moe_cache_get_state": (_S, [_H, _I, _P, _P, _P, _P]),
@@ -157,6 +158,17 @@ def expert_mlp(wdtype: str, hidden: int, inter: int, top_k: int, x, block_ptrs, 
                h_scratch, y, flags: int = 0, stream=None):
     _check(lib().moe_expert_mlp(WDTYPE[wdtype], hidden, inter, top_k, _ptr(x), _ptr(block_ptrs),
                                 _ptr(w), T, _ptr(h_scratch), _ptr(y), flags, _stream(stream)))
+
+
+NOALLOC_MAX_SCRATCH_FLOATS = 1 << 19
+
+
+def expert_mlp_noalloc(wdtype: str, hidden: int, inter: int, top_k: int, x, block_ptrs, w, T: int,
+                       y, flags: int = 0, stream=None):
+    """moe_expert_mlp without a scratch argument: the library's built-in array holds h."""
+    _check(lib().moe_expert_mlp_noalloc(WDTYPE[wdtype], hidden, inter, top_k, _ptr(x),
+                                        _ptr(block_ptrs), _ptr(w), T, _ptr(y), flags,
+                                        _stream(stream)))
 
 
 class MoECache:

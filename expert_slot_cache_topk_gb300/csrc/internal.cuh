@@ -96,6 +96,9 @@ cudaError_t launch_verify(const int32_t* slot_expert, int N, const uint8_t* pool
                           const uint8_t* host_base, unsigned long long stride,
                           unsigned long long nvec, int* mismatches, cudaStream_t s);
 
+// ---- moe_cache.cu: set the message moe_cache_last_error(NULL) returns ----
+moe_status set_global_error(moe_status st, const char* msg);
+
 // ---- launchers (k_mlp.cu) ----
 cudaError_t mlp_configure(int wdtype, int H, int I, int k);  // smem opt-in, call outside capture
 cudaError_t launch_mlp_up(int wdtype, const MlpArgs& a, cudaStream_t s);

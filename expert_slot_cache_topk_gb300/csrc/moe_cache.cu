@@ -385,6 +385,11 @@ moe_status init_state(moe_cache* c) {
 
 }  // namespace
 
+moe_status moe::set_global_error(moe_status st, const char* msg) {
+  g_create_error = msg ? msg : "";
+  return st;
+}
+
 // ============================================================== C ABI
 
 extern "C" {

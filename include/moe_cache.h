@@ -257,6 +257,27 @@ moe_status moe_expert_mlp(int wdtype, int hidden, int inter, int top_k,
                           int T, float* h_scratch_d, void* y_d, int flags,
                           moe_stream_t stream);
 
+/* Allocation-free variant of moe_expert_mlp (the pages have no counterpart;
+ * this entry point exists for callers of this library that cannot allocate
+ * device memory where they call it: code running under CUDA graph capture,
+ * plugins whose host framework's caching allocator owns all device memory,
+ * and latency-critical loops that must not hit cudaMalloc's implicit device
+ * synchronisation).  Same arguments, arithmetic and results as
+ * moe_expert_mlp, minus h_scratch_d: the intermediate h lives in a 2 MiB
+ * array compiled into the library, which every GPU that loads the library
+ * holds until the process exits.  The call allocates nothing.
+ *  - Rejects T * top_k * inter > MOE_NOALLOC_MAX_SCRATCH_FLOATS (MOE_EINVAL).
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents (nothing in it needs to start at zero); calls whose kernels
+ *    overlap on the GPU race on it -- order them on one stream.
+ *  - The first call on each device looks up the array's device address
+ *    (one-time set-up, with that device current); make it before any stream
+ *    capture. */
+#define MOE_NOALLOC_MAX_SCRATCH_FLOATS (1 << 19)
+moe_status moe_expert_mlp_noalloc(int wdtype, int hidden, int inter, int top_k,
+                                  const void* x_d, const uint64_t* block_ptrs_d, const float* w_d,
+                                  int T, void* y_d, int flags, moe_stream_t stream);
+
 /* End-to-end step from host buffers: copies x_h [T, H] and logits_h
  * [L, T, E] (pinned host recommended) to the device, runs every layer as
  * x <- x + MoE_l(x), copies the final x back to y_h [T, H] and waits for it
