@@ -73,14 +73,14 @@ class ClockSampler:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu: int):
-        self.gpu, self.proc, self.lines = gpu, None, []
+    def __init__(self, gpu: int, interval_ms: int = 500):
+        self.gpu, self.proc, self.lines, self.interval_ms = gpu, None, [], interval_ms
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.gpu)],
+                 "-lms", str(self.interval_ms), "-i", str(self.gpu)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -289,7 +289,7 @@ def run_ours(args, w):
     launches0 = c.info()["kernel_launches"]
     c.set_timing(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(local_rank, args.clock_ms) as clk:
         barrier(world)
         torch.cuda.synchronize(dev)
         ev0.record(stream)
@@ -354,7 +354,7 @@ def run_ours(args, w):
                     "uva_gbs_at_create": info["uva_gbs"]},
             "phases_ms_per_step": {k[:-3]: tm[k] / args.steps for k in ("route_ms", "copy_ms", "up_ms", "down_ms")},
             "cache": {k: st1[k] - st0[k] for k in ("hits", "misses", "evictions", "bypass_steps")},
-            "e2e": {"value": e2e_tok / e2e_sec, "unit": UNIT,
+            "e2e": {"value": (e2e_tok / e2e_sec) if e2e_sec > 0 else None, "unit": UNIT,
                     "h2d_bytes_per_step": int(x_h[0].nbytes + lg_h[0].nbytes),
                     "d2h_bytes_per_step": int(y_h.nbytes)},
             "gpu_launches": int(launches),
@@ -381,6 +381,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="olmoe", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--copy-mode", default="auto", choices=["auto", "uva", "memcpy"])
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling case)")
+    ap.add_argument("--clock-ms", type=int, default=500, help="nvidia-smi sampling interval in ms")
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -388,6 +390,8 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        w = w.with_(layers=args.layers)
     if args.impl == "reference":
         run_reference(args, w)
     else:

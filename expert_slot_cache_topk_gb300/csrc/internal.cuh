@@ -9,7 +9,7 @@
 namespace moe {
 
 constexpr int kPrepThreads = 1024;   // one CTA does the whole per-layer bookkeeping
-constexpr int kMlpThreads = 256;     // 8 warps per CTA in the expert MLP kernels
+constexpr int kMlpThreads = 512;     // 16 warps per CTA, one CTA per SM, in the expert MLP kernels
 constexpr int kCopyThreads = 256;
 constexpr int kCopyVecPerThread = 8; // 8 x 16 B in flight per thread
 constexpr int kCopyChunkVec = kCopyThreads * kCopyVecPerThread;  // 32 KiB per CTA step
@@ -55,6 +55,7 @@ struct PrepArgs {
   int32_t* lists;                    // [LST_COUNT * E]
   int32_t* slot_ids_out;             // [T*k] or null
   unsigned long long* asg_ptr;       // [T*k] or null: expert block pointer per assignment
+  uint8_t* pending;                  // [T*k] or null: 1 if the assignment's expert is copied this step
   unsigned long long pool_base;      // this layer's pool
   unsigned long long scratch_base;   // bypass scratch
   unsigned long long host_base;      // device-usable address of this layer's backing store
@@ -83,6 +84,11 @@ struct MlpArgs {
   int T, k, H, I;
   int residual;
   unsigned long long off_w2, off_s13, off_s2;
+  // Optional split of the up (w13) pass: with `pending` set, only assignments
+  // whose pending flag equals `phase` are processed (0 = expert already in
+  // HBM, 1 = expert copied in this step).  pending == nullptr: all of them.
+  const uint8_t* pending;
+  int phase;
 };
 
 // ---- launchers (k_route_prepare.cu) ----

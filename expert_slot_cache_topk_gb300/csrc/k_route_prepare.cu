@@ -152,14 +152,16 @@ __global__ void __launch_bounds__(kPrepThreads, 1) k_prepare(PrepArgs a) {
   __shared__ long long s_stamp[MOE_MAX_EXPERTS];
   __shared__ int s_victim[MOE_MAX_EXPERTS];
   __shared__ unsigned char s_mark[MOE_MAX_EXPERTS];
+  __shared__ unsigned char s_new[MOE_MAX_EXPERTS];  // expert copied in this step
   __shared__ int s_bad;
 
   const int tid = threadIdx.x;
   const int E = a.E, N = a.N;
   const int n_ids = a.T * a.k;
 
+  const int nthr = blockDim.x;   // >= E, a multiple of 32
   if (a.do_route) {
-    for (int t = tid >> 5; t < a.T; t += kPrepThreads / 32)
+    for (int t = tid >> 5; t < a.T; t += nthr / 32)
       route_dispatch(a.logits + (size_t)t * E, E, a.k, a.renorm, a.ids + (size_t)t * a.k,
                      a.w_out + (size_t)t * a.k);
   }
@@ -168,6 +170,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) k_prepare(PrepArgs a) {
   if (tid == 0) s_bad = 0;
   if (tid < E) {
     s_mark[tid] = 0;
+    s_new[tid] = 0;
     s_map[tid] = a.slot_map[tid];
   }
   if (tid < N) {
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) k_prepare(PrepArgs a) {
     s_stamp[tid] = a.slot_stamp[tid];
   }
   __syncthreads();   // also orders the fused router's ids before they are read
-  for (int i = tid; i < n_ids; i += kPrepThreads) {
+  for (int i = tid; i < n_ids; i += nthr) {
     const int e = a.ids[i];
     if ((unsigned)e >= (unsigned)E) s_bad = 1;
     else s_mark[e] = 1;
@@ -189,9 +192,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) k_prepare(PrepArgs a) {
       h.n_ids = n_ids;
       *a.hdr = h;
     }
-    for (int i = tid; i < n_ids; i += kPrepThreads) {
+    for (int i = tid; i < n_ids; i += nthr) {
       if (a.slot_ids_out) a.slot_ids_out[i] = -1;
       if (a.asg_ptr) a.asg_ptr[i] = 0ull;
+      if (a.pending) a.pending[i] = 0;
     }
     return;
   }
@@ -207,6 +211,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) k_prepare(PrepArgs a) {
   if (nc) {
     a.lists[LST_NONCOLD * E + r_nc] = e;
     s_rank[e] = r_nc;
+    if (D > N) s_new[e] = 1;   // bypass: every non-cold expert is copied to scratch
   }
   if (cold) a.lists[LST_COLD * E + r_c] = e;
 
@@ -247,6 +252,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) k_prepare(PrepArgs a) {
     __syncthreads();
     if (miss) {
       if (ev >= 0) s_map[ev] = -1;
+      s_new[e] = 1;
       s_map[e] = slot;
       s_sexp[slot] = e;
       s_stamp[slot] = (long long)(clk + (unsigned long long)(nh + r_m));
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) k_prepare(PrepArgs a) {
     *a.hdr = h;
   }
 
-  for (int i = tid; i < n_ids; i += kPrepThreads) {
+  for (int i = tid; i < n_ids; i += nthr) {
     const int x = a.ids[i];
     int v;
     unsigned long long p;
@@ -306,6 +312,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) k_prepare(PrepArgs a) {
     }
     if (a.slot_ids_out) a.slot_ids_out[i] = v;
     if (a.asg_ptr) a.asg_ptr[i] = p;
+    if (a.pending) a.pending[i] = s_new[x];
   }
 }
 
@@ -393,7 +400,12 @@ cudaError_t launch_router(const float* logits, int T, int E, int k, int renorm, 
 }
 
 cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s) {
-  k_prepare<<<1, kPrepThreads, 0, s>>>(a);
+  // one thread per expert for the ranking scans, one warp per token for the
+  // fused router (at most 32 warps)
+  int need = a.E > 32 * a.T ? a.E : 32 * a.T;
+  if (need > kPrepThreads) need = kPrepThreads;
+  const int threads = (need + 31) / 32 * 32;
+  k_prepare<<<1, threads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -73,6 +73,7 @@ struct moe_cache {
   RecHdr* hdr_d = nullptr;
   int32_t* lists_d = nullptr;
   unsigned long long* asg_d = nullptr;
+  uint8_t* pend_d = nullptr;
   int32_t* ids_d = nullptr;
   float* w_d = nullptr;
   float* h_d = nullptr;
@@ -191,6 +192,7 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
   a.lists = c->lists_d + (size_t)layer * LST_COUNT * c->E;
   a.slot_ids_out = slot_ids_out;
   a.asg_ptr = c->asg_d;
+  a.pending = c->pend_d;
   a.pool_base = (unsigned long long)(c->pool_d + (size_t)layer * c->N * c->stride);
   a.scratch_base = (unsigned long long)c->scratch_d;
   a.host_base = (unsigned long long)(c->backing_dv + (size_t)layer * c->E * c->stride);
@@ -217,18 +219,34 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
   return MOE_OK;
 }
 
-moe_status run_copies(moe_cache* c, int layer, cudaStream_t s) {
+// After the prepare kernel of a layer step: the missed (or, on bypass, all
+// non-cold) experts are copied on the copy stream, forked from the caller's
+// stream right after prepare and joined back before the expert MLP runs.  (An
+// up pass over the experts already in HBM could overlap the copy, but the
+// one-CTA-per-SM up kernel cannot share SMs with the copy kernel, so the
+// overlap was measured slower; the kernels keep the pass filter for callers
+// that want it.)  `mlp` null = prepare only.
+moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const MlpArgs* mlp) {
   uint8_t* pool = c->pool_d + (size_t)layer * c->N * c->stride;
-  const uint8_t* host_dv = c->backing_dv + (size_t)layer * c->E * c->stride;
-  if (c->copy_mode == MOE_COPY_UVA) {
-    CK(c, cudaEventRecord(c->ev_fork, s));
+  const bool memcpy_mode = c->copy_mode == MOE_COPY_MEMCPY;
+  if (memcpy_mode && capturing(s))
+    return fail(c, MOE_ESTATE, "MOE_COPY_MEMCPY needs a host decision per step and cannot be captured; use MOE_COPY_UVA");
+  CK(c, cudaEventRecord(c->ev_fork, s));
+  bool joined = true;
+  if (memcpy_mode) {
+    // read the copy list back (one small read-back per layer step)
+    CK(c, cudaMemcpyAsync(c->hdr_h, c->hdr_d + layer, sizeof(RecHdr), cudaMemcpyDeviceToHost, s));
+    CK(c, cudaMemcpyAsync(c->lists_h, c->lists_d + (size_t)layer * LST_COUNT * c->E,
+                          sizeof(int32_t) * LST_COUNT * c->E, cudaMemcpyDeviceToHost, s));
+    CK(c, cudaEventRecord(c->ev_sync, s));
+  } else {
     CK(c, cudaStreamWaitEvent(c->copy_stream, c->ev_fork, 0));
     const int ti = tm_begin(c, TM_COPY, c->copy_stream);
     CopyArgs a{};
     a.hdr = c->hdr_d + layer;
     a.lists = c->lists_d + (size_t)layer * LST_COUNT * c->E;
     a.E = c->E;
-    a.host_base = host_dv;
+    a.host_base = c->backing_dv + (size_t)layer * c->E * c->stride;
     a.pool_base = pool;
     a.scratch_base = c->scratch_d;
     a.stride = c->stride;
@@ -237,36 +255,40 @@ moe_status run_copies(moe_cache* c, int layer, cudaStream_t s) {
     c->launches++;
     tm_end(c, TM_COPY, ti, c->copy_stream);
     CK(c, cudaEventRecord(c->ev_join, c->copy_stream));
-    CK(c, cudaStreamWaitEvent(s, c->ev_join, 0));
-    return MOE_OK;
   }
-  // MEMCPY: read the copy list back (one small read-back per layer step), then
-  // one cudaMemcpyAsync per expert on the copy stream.
-  if (capturing(s))
-    return fail(c, MOE_ESTATE, "MOE_COPY_MEMCPY needs a host decision per step and cannot be captured; use MOE_COPY_UVA");
-  CK(c, cudaMemcpyAsync(c->hdr_h, c->hdr_d + layer, sizeof(RecHdr), cudaMemcpyDeviceToHost, s));
-  CK(c, cudaMemcpyAsync(c->lists_h, c->lists_d + (size_t)layer * LST_COUNT * c->E,
-                        sizeof(int32_t) * LST_COUNT * c->E, cudaMemcpyDeviceToHost, s));
-  CK(c, cudaEventRecord(c->ev_sync, s));
-  moe_status st = wait_event_bounded(c, c->ev_sync, 30000);
-  if (st != MOE_OK) return st;
-  const RecHdr h = *c->hdr_h;
-  const int n = h.bypass ? h.n_noncold : h.n_misses;
-  if (n == 0) return MOE_OK;
-  CK(c, cudaEventRecord(c->ev_fork, s));
-  CK(c, cudaStreamWaitEvent(c->copy_stream, c->ev_fork, 0));
-  const int ti = tm_begin(c, TM_COPY, c->copy_stream);
-  const int32_t* src = c->lists_h + (h.bypass ? LST_NONCOLD : LST_MISS_E) * c->E;
-  const int32_t* slot = c->lists_h + LST_MISS_SLOT * c->E;
-  const uint8_t* host = c->backing_h + (size_t)layer * c->E * c->stride;
-  for (int i = 0; i < n; ++i) {
-    uint8_t* dst = h.bypass ? c->scratch_d + (size_t)i * c->stride : pool + (size_t)slot[i] * c->stride;
-    CK(c, cudaMemcpyAsync(dst, host + (size_t)src[i] * c->stride, c->Be, cudaMemcpyHostToDevice,
-                          c->copy_stream));
+  if (memcpy_mode) {
+    moe_status st = wait_event_bounded(c, c->ev_sync, 30000);
+    if (st != MOE_OK) return st;
+    const RecHdr h = *c->hdr_h;
+    const int n = h.bypass ? h.n_noncold : h.n_misses;
+    joined = n > 0;
+    if (n > 0) {
+      // one cudaMemcpyAsync per expert on the copy stream
+      CK(c, cudaStreamWaitEvent(c->copy_stream, c->ev_fork, 0));
+      const int ti = tm_begin(c, TM_COPY, c->copy_stream);
+      const int32_t* src = c->lists_h + (h.bypass ? LST_NONCOLD : LST_MISS_E) * c->E;
+      const int32_t* slot = c->lists_h + LST_MISS_SLOT * c->E;
+      const uint8_t* host = c->backing_h + (size_t)layer * c->E * c->stride;
+      for (int i = 0; i < n; ++i) {
+        uint8_t* dst = h.bypass ? c->scratch_d + (size_t)i * c->stride : pool + (size_t)slot[i] * c->stride;
+        CK(c, cudaMemcpyAsync(dst, host + (size_t)src[i] * c->stride, c->Be, cudaMemcpyHostToDevice,
+                              c->copy_stream));
+      }
+      tm_end(c, TM_COPY, ti, c->copy_stream);
+      CK(c, cudaEventRecord(c->ev_join, c->copy_stream));
+    }
   }
-  tm_end(c, TM_COPY, ti, c->copy_stream);
-  CK(c, cudaEventRecord(c->ev_join, c->copy_stream));
-  CK(c, cudaStreamWaitEvent(s, c->ev_join, 0));
+  if (joined) CK(c, cudaStreamWaitEvent(s, c->ev_join, 0));
+  if (mlp) {
+    int ti = tm_begin(c, TM_UP, s);
+    CK(c, launch_mlp_up(c->wd, *mlp, s));
+    c->launches++;
+    tm_end(c, TM_UP, ti, s);
+    ti = tm_begin(c, TM_DOWN, s);
+    CK(c, launch_mlp_down(c->wd, *mlp, s));
+    c->launches++;
+    tm_end(c, TM_DOWN, ti, s);
+  }
   return MOE_OK;
 }
 
@@ -289,18 +311,6 @@ MlpArgs mlp_args(int wd, int H, int I, int k, const void* x, const unsigned long
   a.off_s13 = w13 + w2;
   a.off_s2 = w13 + w2 + s13;
   return a;
-}
-
-moe_status run_mlp(moe_cache* c, const MlpArgs& a, cudaStream_t s) {
-  int ti = tm_begin(c, TM_UP, s);
-  CK(c, launch_mlp_up(c->wd, a, s));
-  c->launches++;
-  tm_end(c, TM_UP, ti, s);
-  ti = tm_begin(c, TM_DOWN, s);
-  CK(c, launch_mlp_down(c->wd, a, s));
-  c->launches++;
-  tm_end(c, TM_DOWN, ti, s);
-  return MOE_OK;
 }
 
 moe_status measure_copy_modes(moe_cache* c) {
@@ -337,7 +347,7 @@ moe_status measure_copy_modes(moe_cache* c) {
   cudaEventDestroy(b);
   c->memcpy_gbs = bytes / (best_m * 1e-3) / 1e9;
   c->uva_gbs = bytes / (best_u * 1e-3) / 1e9;
-  c->copy_mode = c->uva_gbs >= c->memcpy_gbs ? MOE_COPY_UVA : MOE_COPY_MEMCPY;
+  c->copy_mode = c->memcpy_gbs > 1.15 * c->uva_gbs ? MOE_COPY_MEMCPY : MOE_COPY_UVA;
   return MOE_OK;
 }
 
@@ -353,7 +363,7 @@ void free_all(moe_cache* c) {
   if (c->ev_sync) cudaEventDestroy(c->ev_sync);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->slot_map_d, c->slot_expert_d,
-                 c->slot_stamp_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->ids_d,
+                 c->slot_stamp_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->ids_d,
                  c->w_d, c->h_d, c->err_d, c->verify_d, c->xs_d[0], c->xs_d[1],
                  c->logits_stage_d};
   for (void* p : dev)
@@ -508,6 +518,7 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   CKC(dmalloc((void**)&c->hdr_d, L * sizeof(RecHdr)));
   CKC(dmalloc((void**)&c->lists_d, L * LST_COUNT * E * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->asg_d, TK * sizeof(unsigned long long)));
+  CKC(dmalloc((void**)&c->pend_d, TK));
   CKC(dmalloc((void**)&c->ids_d, TK * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->w_d, TK * sizeof(float)));
   CKC(dmalloc((void**)&c->h_d, TK * c->I * sizeof(float)));
@@ -531,7 +542,6 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   c->copy_mode = g.copy_mode;
   if (g.copy_mode == MOE_COPY_AUTO) {
     if (measure_copy_modes(c) != MOE_OK) return bail(MOE_ECUDA);
-    c->copy_mode = (c->uva_gbs >= c->memcpy_gbs) ? MOE_COPY_UVA : MOE_COPY_MEMCPY;
   }
   CKC(cudaDeviceSynchronize());
 #undef CKC
@@ -610,7 +620,7 @@ moe_status moe_cache_prepare(moe_cache_t* c, int layer, const int32_t* ids_d, in
   cudaStream_t s = (cudaStream_t)stream;
   st = run_prepare(c, layer, nullptr, ids_d, T, slot_ids_d, s);
   if (st != MOE_OK) return st;
-  return run_copies(c, layer, s);
+  return run_copies_and_mlp(c, layer, s, nullptr);
 }
 
 moe_status moe_cache_last_prepare(moe_cache_t* c, int layer, moe_prepare_info* out) {
@@ -657,10 +667,8 @@ moe_status moe_forward(moe_cache_t* c, int layer, const void* x_d, const float* 
   cudaStream_t s = (cudaStream_t)stream;
   st = run_prepare(c, layer, logits_d, nullptr, T, nullptr, s);
   if (st != MOE_OK) return st;
-  st = run_copies(c, layer, s);
-  if (st != MOE_OK) return st;
   const MlpArgs a = mlp_args(c->wd, c->H, c->I, c->K, x_d, c->asg_d, c->w_d, c->h_d, y_d, T, flags);
-  return run_mlp(c, a, s);
+  return run_copies_and_mlp(c, layer, s, &a);
 }
 
 moe_status moe_expert_mlp(int wdtype, int hidden, int inter, int top_k, const void* x_d,

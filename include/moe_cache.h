@@ -74,8 +74,10 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_INT4_G128 = 2 } moe_wdtype;
  *  MOE_COPY_UVA     an SM copy kernel on the copy stream reads the device-side
  *                   miss list and copies from the mapped pinned host store with
  *                   16-byte loads.  No host round trip; graph-capturable.
- *  MOE_COPY_AUTO    at create, time both on the backing store and keep the
- *                   faster (moe_cache_info reports the two bandwidths). */
+ *  MOE_COPY_AUTO    at create, time both on the backing store; keep MEMCPY
+ *                   only if it is more than 15% faster, else UVA (no host
+ *                   round trip per layer, so host-side stalls cannot idle the
+ *                   copy engine).  moe_cache_info reports both bandwidths. */
 typedef enum { MOE_COPY_AUTO = 0, MOE_COPY_MEMCPY = 1, MOE_COPY_UVA = 2 } moe_copy_mode;
 
 typedef enum {
