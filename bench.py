@@ -380,7 +380,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=32)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="olmoe", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--copy-mode", default="auto", choices=["auto", "uva", "memcpy"])
+    ap.add_argument("--copy-mode", default="auto", choices=["auto", "uva", "memcpy", "fused"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling case)")
     ap.add_argument("--clock-ms", type=int, default=500, help="nvidia-smi sampling interval in ms")
     ap.add_argument("--e2e-steps", type=int, default=64)

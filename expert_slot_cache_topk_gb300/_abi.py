@@ -19,8 +19,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoecache
 
 MOE_F32, MOE_BF16, MOE_INT4_G128 = 0, 1, 2
 WDTYPE = {"f32": MOE_F32, "bf16": MOE_BF16, "int4g128": MOE_INT4_G128}
-MOE_COPY_AUTO, MOE_COPY_MEMCPY, MOE_COPY_UVA = 0, 1, 2
-COPY_MODE = {"auto": MOE_COPY_AUTO, "memcpy": MOE_COPY_MEMCPY, "uva": MOE_COPY_UVA}
+MOE_COPY_AUTO, MOE_COPY_MEMCPY, MOE_COPY_UVA, MOE_COPY_FUSED = 0, 1, 2, 3
+COPY_MODE = {"auto": MOE_COPY_AUTO, "memcpy": MOE_COPY_MEMCPY, "uva": MOE_COPY_UVA,
+             "fused": MOE_COPY_FUSED}
 COPY_MODE_NAME = {v: k for k, v in COPY_MODE.items()}
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ETIMEOUT, MOE_ESTATE = 0, -1, -2, -3, -4, -5
 STATUS_NAME = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ENOMEM", -3: "MOE_ECUDA",

@@ -35,7 +35,14 @@ struct RecHdr {
 enum { LST_HITS = 0, LST_MISS_E, LST_MISS_SLOT, LST_MISS_EV, LST_COLD, LST_NONCOLD, LST_COUNT };
 
 // Device error flag values (sticky until reset)
-enum { DEVERR_NONE = 0, DEVERR_BAD_ID = 1 };
+enum { DEVERR_NONE = 0, DEVERR_BAD_ID = 1, DEVERR_BARRIER = 2 };
+
+// Grid-wide barrier state of the fused MLP kernel (count returns to 0 after
+// every barrier; gen counts completed barriers).
+struct GridBar {
+  unsigned count;
+  unsigned gen;
+};
 
 struct PrepArgs {
   // fused router (do_route != 0): logits [T, E] -> ids / w
@@ -55,6 +62,7 @@ struct PrepArgs {
   int32_t* lists;                    // [LST_COUNT * E]
   int32_t* slot_ids_out;             // [T*k] or null
   unsigned long long* asg_ptr;       // [T*k] or null: expert block pointer per assignment
+  unsigned long long* src_ptr;       // [T*k] or null: the expert's pinned host block
   uint8_t* pending;                  // [T*k] or null: 1 if the assignment's expert is copied this step
   unsigned long long pool_base;      // this layer's pool
   unsigned long long scratch_base;   // bypass scratch
@@ -84,11 +92,18 @@ struct MlpArgs {
   int T, k, H, I;
   int residual;
   unsigned long long off_w2, off_s13, off_s2;
-  // Optional split of the up (w13) pass: with `pending` set, only assignments
-  // whose pending flag equals `phase` are processed (0 = expert already in
-  // HBM, 1 = expert copied in this step).  pending == nullptr: all of them.
+  // Optional split of the up (w13) pass: with `pending` set and phase >= 0,
+  // only assignments whose pending flag equals `phase` are processed (0 =
+  // expert already in HBM, 1 = expert copied in this step); otherwise all.
   const uint8_t* pending;
   int phase;
+  // Read-through (fused kernel only): assignments whose expert is pending are
+  // read from src_ptr (pinned host block) and written into asg_ptr (their
+  // slot) while computing; bytes [tail_off, tail_off + tail_bytes) of each
+  // pending block (w2 and scales) are copied by extra tasks.
+  const unsigned long long* src_ptr;
+  int readthrough;
+  unsigned long long tail_off, tail_bytes;
 };
 
 // ---- launchers (k_route_prepare.cu) ----
@@ -109,6 +124,8 @@ moe_status set_global_error(moe_status st, const char* msg);
 cudaError_t mlp_configure(int wdtype, int H, int I, int k);  // smem opt-in, call outside capture
 cudaError_t launch_mlp_up(int wdtype, const MlpArgs& a, cudaStream_t s);
 cudaError_t launch_mlp_down(int wdtype, const MlpArgs& a, cudaStream_t s);
+// Up + down in one cooperative launch; cudaErrorNotSupported = use up/down.
+cudaError_t launch_mlp_fused(int wdtype, const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s);
 size_t mlp_down_smem_bytes(int k, int I);
 size_t mlp_up_smem_bytes(int H);
 

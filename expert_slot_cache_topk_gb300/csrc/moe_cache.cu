@@ -73,12 +73,14 @@ struct moe_cache {
   RecHdr* hdr_d = nullptr;
   int32_t* lists_d = nullptr;
   unsigned long long* asg_d = nullptr;
+  unsigned long long* src_d = nullptr;   // host block of each assignment's expert
   uint8_t* pend_d = nullptr;
   int32_t* ids_d = nullptr;
   float* w_d = nullptr;
   float* h_d = nullptr;
   int* err_d = nullptr;
   int* verify_d = nullptr;
+  GridBar* bar_d = nullptr;       // grid barrier of the fused MLP kernel
   RecHdr* hdr_h = nullptr;        // pinned mirror for MEMCPY mode
   int32_t* lists_h = nullptr;
   uint8_t* xs_d[2] = {nullptr, nullptr};
@@ -171,6 +173,8 @@ moe_status device_error(moe_cache* c) {
   CK(c, cudaMemcpy(&e, c->err_d, sizeof(int), cudaMemcpyDeviceToHost));
   if (e == DEVERR_BAD_ID)
     return fail(c, MOE_ESTATE, "device error: an expert id outside [0, E) reached prepare; that step was skipped");
+  if (e == DEVERR_BARRIER)
+    return fail(c, MOE_ESTATE, "device error: the fused MLP kernel's grid barrier timed out; outputs are invalid, call moe_cache_reset");
   return MOE_OK;
 }
 
@@ -192,6 +196,7 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
   a.lists = c->lists_d + (size_t)layer * LST_COUNT * c->E;
   a.slot_ids_out = slot_ids_out;
   a.asg_ptr = c->asg_d;
+  a.src_ptr = c->src_d;
   a.pending = c->pend_d;
   a.pool_base = (unsigned long long)(c->pool_d + (size_t)layer * c->N * c->stride);
   a.scratch_base = (unsigned long long)c->scratch_d;
@@ -228,6 +233,28 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
 // that want it.)  `mlp` null = prepare only.
 moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const MlpArgs* mlp) {
   uint8_t* pool = c->pool_d + (size_t)layer * c->N * c->stride;
+  if (c->copy_mode == MOE_COPY_FUSED && mlp != nullptr && mlp->T == 1) {
+    // read-through: the fused expert-MLP kernel fills the slots itself
+    MlpArgs m = *mlp;
+    m.readthrough = 1;
+    m.pending = c->pend_d;
+    m.src_ptr = c->src_d;
+    m.phase = -1;
+    m.tail_off = c->off_w2;
+    m.tail_bytes = c->Be - c->off_w2;
+    const int ti = tm_begin(c, TM_UP, s);
+    const cudaError_t fe = launch_mlp_fused(c->wd, m, c->bar_d, c->err_d, s);
+    if (fe == cudaSuccess) {
+      c->launches++;
+      tm_end(c, TM_UP, ti, s);
+      return MOE_OK;
+    }
+    if (fe != cudaErrorNotSupported && fe != cudaErrorCooperativeLaunchTooLarge)
+      return cuda_fail(c, fe, "fused expert MLP launch");
+    cudaGetLastError();
+    tm_end(c, TM_UP, ti, s);
+    // no co-resident grid for this shape: copy kernel, then the MLP
+  }
   const bool memcpy_mode = c->copy_mode == MOE_COPY_MEMCPY;
   if (memcpy_mode && capturing(s))
     return fail(c, MOE_ESTATE, "MOE_COPY_MEMCPY needs a host decision per step and cannot be captured; use MOE_COPY_UVA");
@@ -280,7 +307,17 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
   }
   if (joined) CK(c, cudaStreamWaitEvent(s, c->ev_join, 0));
   if (mlp) {
+    // one cooperative launch (up, grid barrier, down); up + down if it cannot fit
     int ti = tm_begin(c, TM_UP, s);
+    const cudaError_t fe = launch_mlp_fused(c->wd, *mlp, c->bar_d, c->err_d, s);
+    if (fe == cudaSuccess) {
+      c->launches++;
+      tm_end(c, TM_UP, ti, s);
+      return MOE_OK;
+    }
+    if (fe != cudaErrorNotSupported && fe != cudaErrorCooperativeLaunchTooLarge)
+      return cuda_fail(c, fe, "fused expert MLP launch");
+    cudaGetLastError();
     CK(c, launch_mlp_up(c->wd, *mlp, s));
     c->launches++;
     tm_end(c, TM_UP, ti, s);
@@ -347,7 +384,7 @@ moe_status measure_copy_modes(moe_cache* c) {
   cudaEventDestroy(b);
   c->memcpy_gbs = bytes / (best_m * 1e-3) / 1e9;
   c->uva_gbs = bytes / (best_u * 1e-3) / 1e9;
-  c->copy_mode = c->memcpy_gbs > 1.15 * c->uva_gbs ? MOE_COPY_MEMCPY : MOE_COPY_UVA;
+  c->copy_mode = c->memcpy_gbs > 1.15 * c->uva_gbs ? MOE_COPY_MEMCPY : MOE_COPY_FUSED;
   return MOE_OK;
 }
 
@@ -363,8 +400,8 @@ void free_all(moe_cache* c) {
   if (c->ev_sync) cudaEventDestroy(c->ev_sync);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->slot_map_d, c->slot_expert_d,
-                 c->slot_stamp_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->ids_d,
-                 c->w_d, c->h_d, c->err_d, c->verify_d, c->xs_d[0], c->xs_d[1],
+                 c->slot_stamp_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
+                 c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->xs_d[0], c->xs_d[1],
                  c->logits_stage_d};
   for (void* p : dev)
     if (p) cudaFree(p);
@@ -390,6 +427,7 @@ moe_status init_state(moe_cache* c) {
   CK(c, cudaMemset(c->hdr_d, 0, L * sizeof(RecHdr)));
   CK(c, cudaMemset(c->lists_d, 0, L * LST_COUNT * E * sizeof(int32_t)));
   CK(c, cudaMemset(c->err_d, 0, sizeof(int)));
+  CK(c, cudaMemset(c->bar_d, 0, sizeof(GridBar)));
   return MOE_OK;
 }
 
@@ -434,7 +472,7 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
     return fail(nullptr, MOE_EINVAL, "bad wdtype or shape (int4 needs hidden, inter multiples of 128)");
   if (g.hidden % chunk_elems(g.wdtype) || g.inter % chunk_elems(g.wdtype))
     return fail(nullptr, MOE_EINVAL, "hidden and inter must be multiples of 4 (f32) or 8 (bf16)");
-  if (g.copy_mode < MOE_COPY_AUTO || g.copy_mode > MOE_COPY_UVA)
+  if (g.copy_mode < MOE_COPY_AUTO || g.copy_mode > MOE_COPY_FUSED)
     return fail(nullptr, MOE_EINVAL, "bad copy_mode");
   if (g.renormalize != 0 && g.renormalize != 1) return fail(nullptr, MOE_EINVAL, "renormalize must be 0 or 1");
   if (mlp_up_smem_bytes(g.hidden) > 200 * 1024 || mlp_down_smem_bytes(g.top_k, g.inter) > 200 * 1024)
@@ -519,10 +557,12 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   CKC(dmalloc((void**)&c->lists_d, L * LST_COUNT * E * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->asg_d, TK * sizeof(unsigned long long)));
   CKC(dmalloc((void**)&c->pend_d, TK));
+  CKC(dmalloc((void**)&c->src_d, TK * sizeof(unsigned long long)));
   CKC(dmalloc((void**)&c->ids_d, TK * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->w_d, TK * sizeof(float)));
   CKC(dmalloc((void**)&c->h_d, TK * c->I * sizeof(float)));
   CKC(dmalloc((void**)&c->err_d, sizeof(int)));
+  CKC(dmalloc((void**)&c->bar_d, sizeof(GridBar)));
   CKC(dmalloc((void**)&c->verify_d, sizeof(int)));
   CKC(dmalloc((void**)&c->xs_d[0], (size_t)c->maxT * c->H * act_bytes(c->wd)));
   CKC(dmalloc((void**)&c->xs_d[1], (size_t)c->maxT * c->H * act_bytes(c->wd)));

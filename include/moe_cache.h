@@ -74,11 +74,21 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_INT4_G128 = 2 } moe_wdtype;
  *  MOE_COPY_UVA     an SM copy kernel on the copy stream reads the device-side
  *                   miss list and copies from the mapped pinned host store with
  *                   16-byte loads.  No host round trip; graph-capturable.
- *  MOE_COPY_AUTO    at create, time both on the backing store; keep MEMCPY
- *                   only if it is more than 15% faster, else UVA (no host
- *                   round trip per layer, so host-side stalls cannot idle the
- *                   copy engine).  moe_cache_info reports both bandwidths. */
-typedef enum { MOE_COPY_AUTO = 0, MOE_COPY_MEMCPY = 1, MOE_COPY_UVA = 2 } moe_copy_mode;
+ *  MOE_COPY_FUSED   single-token steps (decode): no separate copy.  The
+ *                   expert-MLP kernel reads a missed expert's gate/up rows
+ *                   straight from the pinned host store (the host link on
+ *                   GB300 is coherent NVLink-C2C), computes with them and
+ *                   writes them into the victim slot in the same pass; spare
+ *                   warps copy the expert's w2 and scales into the slot at the
+ *                   same time, so host-link traffic overlaps HBM streaming.
+ *                   Steps with T > 1, and moe_cache_prepare, use the UVA copy
+ *                   kernel.  Graph-capturable.
+ *  MOE_COPY_AUTO    at create, time cudaMemcpyAsync and the SM copy kernel on
+ *                   the backing store; MEMCPY if it is more than 15% faster,
+ *                   else FUSED (no host round trip per layer, so host-side
+ *                   stalls cannot idle the copy engine).  moe_cache_info
+ *                   reports both bandwidths and the mode chosen. */
+typedef enum { MOE_COPY_AUTO = 0, MOE_COPY_MEMCPY = 1, MOE_COPY_UVA = 2, MOE_COPY_FUSED = 3 } moe_copy_mode;
 
 typedef enum {
   MOE_OK = 0,
@@ -174,6 +184,9 @@ typedef struct {
 typedef struct {
   double route_ms, copy_ms, up_ms, down_ms;   /* router+prepare, miss/bypass copy, w13, w2 */
   uint64_t route_n, copy_n, up_n, down_n;     /* launches timed */
+  /* moe_forward normally runs w13 and w2 in one fused kernel, timed under
+   * up_ms / up_n (down_n then stays 0); separate up/down launches are timed
+   * under their own fields. */
 } moe_cache_timing;
 
 /* ---------------------------------------------------------------- lifecycle */
@@ -250,9 +263,9 @@ moe_status moe_forward(moe_cache_t* c, int layer, const void* x_d, const float* 
                        int T, void* y_d, int flags, moe_stream_t stream);
 
 /* Grouped expert MLP alone, no cache: for each assignment a = t*k + j,
- * block_ptrs_d[a] is a device-readable pointer to expert e's canonical block
- * (HBM or mapped pinned host; 0 = skip, contributes zero) and w_d[a] its
- * weight.  h_scratch_d is caller-provided scratch of T*k*I floats.  Same
+ * block_ptrs_d[a] is a device-readable, 16-byte aligned pointer to expert e's
+ * canonical block (HBM or mapped pinned host; 0 = skip, contributes zero) and
+ * w_d[a] its weight.  h_scratch_d is caller-provided scratch of T*k*I floats.  Same
  * arithmetic and summation order as moe_forward. */
 moe_status moe_expert_mlp(int wdtype, int hidden, int inter, int top_k,
                           const void* x_d, const uint64_t* block_ptrs_d, const float* w_d,

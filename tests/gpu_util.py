@@ -10,9 +10,14 @@ from expert_slot_cache_topk_gb300 import synth
 from expert_slot_cache_topk_gb300._abi import MoECache
 from oracle import LayerSlotCache, dequant_expert, expert_nbytes, moe_combine, router_topk
 
-# float tolerance of the spec contract, applied elementwise as
-# |gpu - oracle| <= ATOL + RTOL * |oracle|
+# float tolerance of the spec contract for bf16 / INT4 weights, applied
+# elementwise as |gpu - oracle| <= ATOL + RTOL * |oracle|
 ATOL, RTOL = 2e-2, 1e-2
+# f32 weights (the tiny workload) compute and store in f32: the only error is
+# f32 rounding of dot products of length <= 128 and of the exp in silu, far
+# below 1e-5 relative; outputs there are ~3e-3, so the bf16 absolute bound
+# would not see a wrong answer.
+ATOL_F32, RTOL_F32 = 1e-7, 1e-4
 
 
 def make_cache(w: synth.Workload, copy_mode="uva", slots=None, max_tokens=None, cold=None,
@@ -70,9 +75,9 @@ def oracle_y(w: synth.Workload, weights: OracleWeights, layer: int, x: np.ndarra
     return moe_combine(x_to_f64(w, x), ids, wts, lambda e: weights(layer, e))
 
 
-def assert_close(got: np.ndarray, ref: np.ndarray, what=""):
+def assert_close(got: np.ndarray, ref: np.ndarray, what="", f32=False):
     err = np.abs(got - ref)
-    bound = ATOL + RTOL * np.abs(ref)
+    bound = (ATOL_F32 + RTOL_F32 * np.abs(ref)) if f32 else (ATOL + RTOL * np.abs(ref))
     bad = err > bound
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance, "
                            f"max err {err.max():.3e}, worst at {np.unravel_index(np.argmax(err - bound), err.shape)}")

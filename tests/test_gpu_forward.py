@@ -29,15 +29,18 @@ def _forward_steps(c, w, layer, xs, lgs, flags=0):
     return ys
 
 
-@pytest.mark.parametrize("name,L,steps,slots", [
-    ("tiny", 1, 64, None),
-    ("olmoe", 2, 10, None),
-    ("int4", 2, 10, 16),
-    ("int4", 1, 6, 0),
+@pytest.mark.parametrize("name,L,steps,slots,mode", [
+    ("tiny", 1, 64, None, "uva"),
+    ("tiny", 1, 64, None, "fused"),
+    ("olmoe", 2, 10, None, "uva"),
+    ("olmoe", 2, 10, None, "fused"),
+    ("int4", 2, 10, 16, "fused"),
+    ("int4", 1, 6, 0, "uva"),
+    ("int4", 1, 6, 0, "fused"),
 ])
-def test_forward_matches_oracle(name, L, steps, slots):
+def test_forward_matches_oracle(name, L, steps, slots, mode):
     w = W[name].with_(layers=L)
-    c = make_cache(w, slots=slots)
+    c = make_cache(w, slots=slots, copy_mode=mode)
     wt = OracleWeights(w)
     for l in range(L):
         lgs = synth.routing_logits(w, l, steps)
@@ -45,7 +48,7 @@ def test_forward_matches_oracle(name, L, steps, slots):
         ys = _forward_steps(c, w, l, xs, lgs)
         for s in range(steps):
             ref = oracle_y(w, wt, l, xs[s], lgs[s])
-            assert_close(y_to_f64(w, ys[s]), ref, f"{name} layer {l} step {s}")
+            assert_close(y_to_f64(w, ys[s]), ref, f"{name} layer {l} step {s}", f32=w.wdtype == "f32")
     c.check()
     c.close()
 
@@ -105,6 +108,9 @@ def test_cached_resident_bypass_cold_bitwise_equal(name):
         "bypass": dict(slots=0),
         "cold": dict(slots=w.top_k, cold=np.ones((1, w.experts), np.uint8)),
         "memcpy": dict(slots=w.top_k + 2, copy_mode="memcpy"),
+        "fused": dict(slots=w.top_k + 2, copy_mode="fused"),
+        "fused_bypass": dict(slots=0, copy_mode="fused"),
+        "fused_resident": dict(slots=w.experts, copy_mode="fused"),
     }
     for key, kw in variants.items():
         c = make_cache(w, **kw)
@@ -117,9 +123,10 @@ def test_cached_resident_bypass_cold_bitwise_equal(name):
             assert (outs[key][s] == outs["cached"][s]).all(), (key, s)
 
 
-def test_slots_hold_their_experts_after_churn():
+@pytest.mark.parametrize("mode", ["uva", "fused", "memcpy"])
+def test_slots_hold_their_experts_after_churn(mode):
     w = W["int4"].with_(layers=2, hidden=256, inter=128)
-    c = make_cache(w, slots=12)
+    c = make_cache(w, slots=12, copy_mode=mode)
     for l in range(2):
         _forward_steps(c, w, l, synth.hidden_states(w, l, 40), synth.routing_logits(w, l, 40))
         assert c.verify_slots(l) == 0
@@ -145,7 +152,7 @@ def test_load_expert_refreshes_a_resident_slot():
     wt = OracleWeights(w)
     from oracle import dequant_expert
     wt.cache[(0, e)] = dequant_expert(blk, w.wdtype, w.hidden, w.inter)
-    assert_close(y_to_f64(w, y), oracle_y(w, wt, 0, xs[0], lgs[0]), "after reload")
+    assert_close(y_to_f64(w, y), oracle_y(w, wt, 0, xs[0], lgs[0]), "after reload", f32=True)
     c.close()
 
 
@@ -176,7 +183,8 @@ def test_residual_flag_and_expert_mlp_entry_point():
     c.close()
 
 
-def test_graph_capture_uva_replays_like_eager():
+@pytest.mark.parametrize("mode", ["uva", "fused"])
+def test_graph_capture_replays_like_eager(mode):
     import torch
     w = W["olmoe"].with_(layers=2, hidden=512, inter=256)
     steps = 6
@@ -184,7 +192,7 @@ def test_graph_capture_uva_replays_like_eager():
     xs = [synth.hidden_states(w, l, steps) for l in range(2)]
     ref = make_cache(w, slots=10)
     ref_y = [[y.clone() for y in _forward_steps(ref, w, l, xs[l], lgs[l])] for l in range(2)]
-    c = make_cache(w, slots=10)
+    c = make_cache(w, slots=10, copy_mode=mode)
     x_st = [torch_x(w, xs[l][0]).clone() for l in range(2)]
     lg_st = [torch.from_numpy(lgs[l][0]).cuda() for l in range(2)]
     y_st = [empty_y(w, 1) for _ in range(2)]

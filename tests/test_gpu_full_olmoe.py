@@ -1,6 +1,6 @@
 """Full-size OLMoE-shaped workload (16 layers x 64 experts, top-8, H 2048,
 I 1024, bf16, 16 slots per layer) in the launch configuration the benchmark
-times (UVA copy mode, batch 1): every layer step's slot trace bit-exact
+times (the AUTO copy mode, batch 1): every layer step's slot trace bit-exact
 against the oracle, and sampled (step, layer) outputs against the float64
 oracle.  Layers are fed independent seeded hidden states so each sampled
 output has an oracle input that never came from the GPU."""
@@ -20,7 +20,7 @@ def test_olmoe_full_size_trace_and_sampled_outputs():
     import torch
     w = synth.WORKLOADS["olmoe"]
     steps = 48
-    c = make_cache(w, copy_mode="uva")
+    c = make_cache(w, copy_mode="auto")
     oc = oracle_slot_caches(w)
     lgs = [synth.routing_logits(w, l, steps) for l in range(w.layers)]
     xs = [synth.hidden_states(w, l, steps) for l in range(w.layers)]

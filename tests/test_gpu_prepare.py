@@ -22,7 +22,7 @@ def _prepare(c, layer, ids_np):
     return out
 
 
-@pytest.mark.parametrize("copy_mode", ["uva", "memcpy"])
+@pytest.mark.parametrize("copy_mode", ["uva", "memcpy", "fused"])
 @pytest.mark.parametrize("tr", TRACES, ids=[t.name for t in TRACES])
 def test_golden_trace_on_gpu(tr, copy_mode):
     from expert_slot_cache_topk_gb300._abi import MoECache
