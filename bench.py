@@ -143,6 +143,20 @@ def peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+# DRAM bytes per launch of the roofline kernel from an ncu capture
+# (profiles/k_mlp_fused_olmoe_decode_nomiss.md), valid only while the kernel
+# source is the one that was profiled.
+MEASURED_TRAFFIC = {
+    ("olmoe", "k_mlp.cu:f2cd2368a515f0c8"): 101_358_848,
+}
+
+
+def kernel_source_tag() -> str:
+    import hashlib
+    with open(os.path.join(ROOT, "expert_slot_cache_topk_gb300", "csrc", "k_mlp.cu"), "rb") as f:
+        return "k_mlp.cu:" + hashlib.sha256(f.read()).hexdigest()[:16]
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -246,6 +260,15 @@ def run_reference(args, w):
 # our arm
 # ---------------------------------------------------------------------------
 
+def _fit_per_miss(ms: np.ndarray, misses: np.ndarray):
+    """Least-squares fit ms = base + per_miss * misses over the timed MLP launches."""
+    if len(ms) < 2 or misses.max() == misses.min():
+        return None, None
+    A = np.stack([np.ones(len(ms)), misses.astype(np.float64)], 1)
+    base, per = np.linalg.lstsq(A, ms.astype(np.float64), rcond=None)[0]
+    return float(base), float(per)
+
+
 def run_ours(args, w):
     import torch
     from expert_slot_cache_topk_gb300 import _build
@@ -271,50 +294,70 @@ def run_ours(args, w):
     x0 = synth.hidden_states(w, 0, S)                                                 # [S, T, H]
     lg_d = torch.from_numpy(lg).to(dev)
     x0_d = torch.from_numpy(x0.view(np.int16)).to(dev).view(torch.bfloat16)
-    bufs = [torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    stream = torch.cuda.current_stream(dev)
+    # every step has its own output buffers, so a graph of all timed steps needs no copies
+    ys = torch.empty((S, w.layers, w.tokens, w.hidden), dtype=torch.bfloat16, device=dev)
 
-    def step(s):
+    def step(s, stream):
         x = x0_d[s]
         for l in range(w.layers):
-            y = bufs[l & 1]
-            c.forward(l, x, lg_d[s, l], w.tokens, y, MOE_FWD_RESIDUAL, stream)
-            x = y
-        return x
+            c.forward(l, x, lg_d[s, l], w.tokens, ys[s, l], MOE_FWD_RESIDUAL, stream)
+            x = ys[s, l]
 
-    for s in range(args.warmup):
-        step(s)
-    torch.cuda.synchronize(dev)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.current_stream(dev).synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            step(s, stream)
+    stream.synchronize()
     st0 = c.stats(-1)
     launches0 = c.info()["kernel_launches"]
-    c.set_timing(True)
+    c.set_timing(True, capacity=args.steps * w.layers + 64)
+    graph = None
+    # MEMCPY mode takes a host decision per layer step, so it cannot be captured
+    if not args.no_graph and info["copy_mode_name"] != "memcpy":
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for s in range(args.warmup, S):
+                    step(s, stream)
+        stream.synchronize()
+    launches = c.info()["kernel_launches"] - launches0
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank, args.clock_ms) as clk:
         barrier(world)
         torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        for s in range(args.warmup, S):
-            step(s)
-        ev1.record(stream)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                for s in range(args.warmup, S):
+                    step(s, stream)
+            ev1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
     sec = ev0.elapsed_time(ev1) / 1e3
+    if graph is None:
+        launches = c.info()["kernel_launches"] - launches0
     tm = c.read_timing()
+    mlp_ms, mlp_miss = c.read_timing_launches()
     c.set_timing(False)
     st1 = c.stats(-1)
-    launches = c.info()["kernel_launches"] - launches0
     tokens = args.steps * w.tokens
     max_sec, all_tokens = aggregate(sec, tokens, world, dev)
 
-    # algorithmic bytes of the up (w13) kernel: k experts' w13 (+ scales) per launch
+    # roofline of the expert-MLP kernel over the launches with no miss: every
+    # byte of the k experts' blocks is read from HBM once per launch
     lay = synth.expert_layout(w.wdtype, w.hidden, w.inter)
-    up_bytes = w.tokens * w.top_k * (lay["w13"][1] + lay["s13"][1])     # batch 1: every expert read once
-    up_ms = tm["up_ms"] / max(tm["up_n"], 1)
+    bytes_hbm = w.tokens * w.top_k * lay["total"]
     pk = peaks()
-    achieved = up_bytes / (up_ms * 1e-3) / 1e9
+    hit_ms = mlp_ms[(mlp_miss == 0) & (mlp_ms > 0)]
+    hit_us = float(hit_ms.mean() * 1e3) if len(hit_ms) else None
+    achieved = bytes_hbm / (hit_us * 1e-6) / 1e9 if hit_us else None
+    base_ms, per_miss_ms = _fit_per_miss(mlp_ms[mlp_ms > 0], mlp_miss[mlp_ms > 0])
+    miss_gbs = lay["total"] / (per_miss_ms * 1e-3) / 1e9 if per_miss_ms and per_miss_ms > 0 else None
     miss_bytes = st1["bytes_h2d_miss"] - st0["bytes_h2d_miss"] + st1["bytes_h2d_bypass"] - st0["bytes_h2d_bypass"]
-    copy_s = tm["copy_ms"] / 1e3
-    h2d_peak = max(info["memcpy_gbs"], info["uva_gbs"]) if args.copy_mode == "auto" else None
+    h2d_peak = max(info["memcpy_gbs"], info["uva_gbs"]) or None
 
     # end-to-end through the C ABI with host buffers (copies inside the timed region)
     e2e_steps = min(args.e2e_steps, S)
@@ -328,7 +371,6 @@ def run_ours(args, w):
     e2e_s = time.perf_counter() - t0
     e2e_sec, e2e_tok = aggregate(e2e_s, e2e_steps * w.tokens, world, dev)
 
-    line = None
     if rank == 0:
         cpu_v, cpu_n, cpu_dt = (None, 0, 0.0)
         if world == 1 and not args.no_cpu_baseline:
@@ -339,22 +381,24 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded Zipf routing with reuse; N(0,0.02) weights)",
             "config": {"workload": workload_desc(w), "tokens_per_step": w.tokens,
-                       "copy_mode": info["copy_mode_name"], "graph": False,
+                       "copy_mode": info["copy_mode_name"], "graph": graph is not None,
                        "l2": "inputs larger than L2: every step reads "
                              f"{w.layers * w.top_k * lay['total'] / 1e9:.2f} GB of expert weights",
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "k_up (w13 + SiLU-mul)", "achieved": achieved,
-                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                         "traffic": None, "peak_source": pk["source"],
-                         "bytes_per_launch": up_bytes, "avg_launch_us": up_ms * 1e3,
-                         "launches": tm["up_n"]},
-            "h2d": {"miss_bytes": miss_bytes, "copy_ms_total": tm["copy_ms"],
-                    "miss_gbs": (miss_bytes / copy_s / 1e9) if copy_s > 0 else None,
-                    "peak_gbs": h2d_peak, "memcpy_gbs_at_create": info["memcpy_gbs"],
-                    "uva_gbs_at_create": info["uva_gbs"]},
+            "roofline": {"bound": "hbm", "kernel": "k_mlp_fused (w13 + SiLU-mul + w2, launches with no miss)",
+                         "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
+                         "traffic": MEASURED_TRAFFIC.get((w.name, kernel_source_tag())),
+                         "peak_source": pk["source"], "bytes_per_launch": bytes_hbm,
+                         "avg_launch_us": hit_us, "launches": int(len(hit_ms))},
+            "h2d": {"miss_bytes": miss_bytes, "miss_gbs": miss_gbs,
+                    "per_miss_us": per_miss_ms * 1e3 if per_miss_ms else None,
+                    "mlp_base_us": base_ms * 1e3 if base_ms is not None else None,
+                    "peak_gbs": h2d_peak, "frac": (miss_gbs / h2d_peak) if (miss_gbs and h2d_peak) else None,
+                    "how": "slope of MLP-launch time vs misses in that layer step (least squares)"},
             "phases_ms_per_step": {k[:-3]: tm[k] / args.steps for k in ("route_ms", "copy_ms", "up_ms", "down_ms")},
             "cache": {k: st1[k] - st0[k] for k in ("hits", "misses", "evictions", "bypass_steps")},
-            "e2e": {"value": (e2e_tok / e2e_sec) if e2e_sec > 0 else None, "unit": UNIT,
+            "e2e": {"value": (e2e_tok / e2e_sec) if e2e_steps > 0 else None, "unit": UNIT,
                     "h2d_bytes_per_step": int(x_h[0].nbytes + lg_h[0].nbytes),
                     "d2h_bytes_per_step": int(y_h.nbytes)},
             "gpu_launches": int(launches),
@@ -366,6 +410,7 @@ def run_ours(args, w):
                                     "sample": f"{cpu_n} (token, layer) steps of the first 2 decode tokens "
                                               f"in {cpu_dt:.1f} s (float64 numpy, BLAS threads as installed)"}
         print(json.dumps(line), flush=True)
+    del graph
     c.close()
     if world > 1:
         import torch.distributed as dist
@@ -382,10 +427,11 @@ def main():
     ap.add_argument("--workload", default="olmoe", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--copy-mode", default="auto", choices=["auto", "uva", "memcpy", "fused"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling case)")
-    ap.add_argument("--clock-ms", type=int, default=500, help="nvidia-smi sampling interval in ms")
+    ap.add_argument("--clock-ms", type=int, default=100, help="nvidia-smi sampling interval in ms")
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -95,8 +95,9 @@ SIGNATURES = {
     "moe_cache_pool_ptrs": (_S, [_H, _I, C.POINTER(_P), C.POINTER(_P)]),
     "moe_cache_check": (_S, [_H]),
     "moe_cache_reset": (_S, [_H]),
-    "moe_cache_set_timing": (_S, [_H, _I]),
+    "moe_cache_set_timing": (_S, [_H, _I, _I]),
     "moe_cache_read_timing": (_S, [_H, C.POINTER(moe_cache_timing)]),
+    "moe_cache_read_timing_launches": (_S, [_H, _P, _P, _I, C.POINTER(_I)]),
 }
 
 _lib = None
@@ -301,8 +302,17 @@ class MoECache:
     def reset(self):
         self._ck(lib().moe_cache_reset(self._h))
 
-    def set_timing(self, on: bool):
-        self._ck(lib().moe_cache_set_timing(self._h, int(bool(on))))
+    def set_timing(self, on: bool, capacity: int = 0):
+        self._ck(lib().moe_cache_set_timing(self._h, int(bool(on)), capacity))
+
+    def read_timing_launches(self, cap: int = 1 << 16):
+        """(ms per timed MLP launch, misses of that layer step) as numpy arrays."""
+        ms = np.zeros(cap, np.float32)
+        mi = np.zeros(cap, np.int32)
+        n = C.c_int()
+        self._ck(lib().moe_cache_read_timing_launches(self._h, ms.ctypes.data, mi.ctypes.data, cap,
+                                                      C.byref(n)))
+        return ms[: n.value], mi[: n.value]
 
     def read_timing(self) -> dict:
         t = moe_cache_timing()

@@ -33,6 +33,8 @@ struct TimingPool {
   size_t used = 0;
 };
 
+constexpr int kDefaultTimingCap = 4096;
+
 size_t round_up(size_t v, size_t m) { return (v + m - 1) / m * m; }
 
 bool layout(int wd, int H, int I, size_t* w13, size_t* w2, size_t* s13, size_t* s2) {
@@ -93,6 +95,8 @@ struct moe_cache {
   unsigned long long launches = 0;
   bool timing_on = false;
   TimingPool tp[TM_COUNT];
+  int32_t* tm_miss_d = nullptr;   // per timed MLP launch: misses of that layer step
+  size_t tm_miss_cap = 0;
   std::string err;
 };
 
@@ -146,6 +150,13 @@ void tm_end(moe_cache* c, int cat, int idx, cudaStream_t s) {
   if (idx < 0) return;
   if (capturing(s)) cudaEventRecordWithFlags(c->tp[cat].end[idx], s, cudaEventRecordExternal);
   else cudaEventRecord(c->tp[cat].end[idx], s);
+}
+
+// After a timed MLP launch: copy that layer step's miss count next to its
+// events (a device-to-device copy, so graph replays refresh it too).
+void tm_note_misses(moe_cache* c, int idx, int layer, cudaStream_t s) {
+  if (idx < 0 || c->tm_miss_d == nullptr || (size_t)idx >= c->tm_miss_cap) return;
+  cudaMemcpyAsync(c->tm_miss_d + idx, &c->hdr_d[layer].n_misses, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
 }
 
 moe_status wait_event_bounded(moe_cache* c, cudaEvent_t ev, int timeout_ms) {
@@ -247,6 +258,7 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
     if (fe == cudaSuccess) {
       c->launches++;
       tm_end(c, TM_UP, ti, s);
+      tm_note_misses(c, ti, layer, s);
       return MOE_OK;
     }
     if (fe != cudaErrorNotSupported && fe != cudaErrorCooperativeLaunchTooLarge)
@@ -313,6 +325,7 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
     if (fe == cudaSuccess) {
       c->launches++;
       tm_end(c, TM_UP, ti, s);
+      tm_note_misses(c, ti, layer, s);
       return MOE_OK;
     }
     if (fe != cudaErrorNotSupported && fe != cudaErrorCooperativeLaunchTooLarge)
@@ -321,6 +334,7 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
     CK(c, launch_mlp_up(c->wd, *mlp, s));
     c->launches++;
     tm_end(c, TM_UP, ti, s);
+    tm_note_misses(c, ti, layer, s);
     ti = tm_begin(c, TM_DOWN, s);
     CK(c, launch_mlp_down(c->wd, *mlp, s));
     c->launches++;
@@ -401,7 +415,7 @@ void free_all(moe_cache* c) {
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->slot_map_d, c->slot_expert_d,
                  c->slot_stamp_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
-                 c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->xs_d[0], c->xs_d[1],
+                 c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->tm_miss_d, c->xs_d[0], c->xs_d[1],
                  c->logits_stage_d};
   for (void* p : dev)
     if (p) cudaFree(p);
@@ -852,13 +866,15 @@ moe_status moe_cache_reset(moe_cache_t* c) {
   return MOE_OK;
 }
 
-moe_status moe_cache_set_timing(moe_cache_t* c, int on) {
+moe_status moe_cache_set_timing(moe_cache_t* c, int on, int capacity) {
   if (!c) return fail(nullptr, MOE_EINVAL, "null handle");
+  if (capacity < 0 || capacity > (1 << 22)) return fail(c, MOE_EINVAL, "timing capacity out of range");
   CK(c, cudaSetDevice(c->cfg.device));
+  const size_t cap = capacity ? (size_t)capacity : (size_t)kDefaultTimingCap;
   for (auto& p : c->tp) {
     p.used = 0;
     if (on) {
-      while (p.beg.size() < 4096) {
+      while (p.beg.size() < cap) {
         cudaEvent_t a, b;
         CK(c, cudaEventCreate(&a));
         CK(c, cudaEventCreate(&b));
@@ -867,7 +883,38 @@ moe_status moe_cache_set_timing(moe_cache_t* c, int on) {
       }
     }
   }
+  if (on && c->tm_miss_cap < cap) {
+    if (c->tm_miss_d) CK(c, cudaFree(c->tm_miss_d));
+    c->tm_miss_d = nullptr;
+    CK(c, cudaMalloc((void**)&c->tm_miss_d, cap * sizeof(int32_t)));
+    c->tm_miss_cap = cap;
+  }
   c->timing_on = on != 0;
+  return MOE_OK;
+}
+
+moe_status moe_cache_read_timing_launches(moe_cache_t* c, float* ms_h, int32_t* misses_h, int cap,
+                                          int* n) {
+  if (!c || !n || cap < 0) return fail(c, MOE_EINVAL, "null argument");
+  CK(c, cudaSetDevice(c->cfg.device));
+  CK(c, cudaDeviceSynchronize());
+  const TimingPool& p = c->tp[TM_UP];
+  const int avail = (int)p.used;
+  const int m = avail < cap ? avail : cap;
+  std::vector<int32_t> mi(m > 0 ? m : 1, 0);
+  const int mc = m < (int)c->tm_miss_cap ? m : (int)c->tm_miss_cap;
+  if (mc > 0 && c->tm_miss_d)
+    CK(c, cudaMemcpy(mi.data(), c->tm_miss_d, (size_t)mc * sizeof(int32_t), cudaMemcpyDeviceToHost));
+  for (int i = 0; i < m; ++i) {
+    float v = -1.f;
+    if (cudaEventElapsedTime(&v, p.beg[i], p.end[i]) != cudaSuccess) {
+      cudaGetLastError();
+      v = -1.f;
+    }
+    if (ms_h) ms_h[i] = v;
+    if (misses_h) misses_h[i] = mi[i];
+  }
+  *n = m;
   return MOE_OK;
 }
 

@@ -1,0 +1,346 @@
+// Router top-k and per-layer slot bookkeeping as device functions, shared by
+// the standalone prepare kernel (k_route_prepare.cu) and the fused per-layer
+// kernel (k_mlp.cu), so both run the same code.
+//
+// Router: one warp per token; a logit is turned into an order-preserving
+// 32-bit key, and each of the k rounds takes two warp max-reductions (largest
+// key, then among equal keys the lowest id), so ties go to the lower id
+// ("Running 125B MoE on Two 32 GB Cards", section 4.2).
+//
+// Prepare: one CTA with one thread per expert keeps the whole LRU in shared
+// memory.  Distinct experts are found with a shared-memory hit table and ranked
+// with warp ballots (five flags in one block scan), so the result equals an
+// OrderedDict LRU processed in ascending id order (vLLM PR #37190 "Run MoE
+// models exceeding VRAM via expert CPU offloading with GPU cache", "How it
+// works"), with hits touched before misses are filled.  Bypass when the
+// distinct non-cold experts exceed the slots (llama.cpp discussion #28248
+// "RFC: Persistent expert slot pool for MoE CPU offload", "Why not the other
+// approaches on the table").  Latency-bound: every global read is issued up
+// front and the routed ids stay in shared memory.
+#pragma once
+
+#include <climits>
+#include <cstdint>
+
+#include "internal.cuh"
+
+namespace moe {
+namespace prep {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr int kMaxRoutedIds = 64 * MOE_MAX_TOPK;   // in-kernel router: T <= 64
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+  return v;
+}
+
+// Order-preserving key of a logit: larger logit -> larger key.  NaN ranks as
+// -inf, and -0.0 equals +0.0 (they compare equal, so the lower id wins).
+__device__ __forceinline__ unsigned logit_key(float v) {
+  if (v != v) v = -INFINITY;
+  if (v == 0.0f) v = 0.0f;
+  const unsigned b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Top-k of one token's logits by one warp.  Lane l holds logits l + 32 i.
+// Writes ids / w to global and, when s_ids is given, ids to shared memory.
+template <int PL>
+__device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k, int renorm,
+                            int32_t* __restrict__ ids, float* __restrict__ w, int32_t* s_ids) {
+  const int lane = threadIdx.x & 31;
+  unsigned key[PL];
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = (e < E) ? logit_key(row[e]) : 0u;
+  }
+  unsigned km = 0;
+#pragma unroll
+  for (int i = 0; i < PL; ++i) km = key[i] > km ? key[i] : km;
+  const float m = key_logit(__reduce_max_sync(kFullMask, km));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < PL; ++i)
+    if (lane + 32 * i < E) s += expf(key_logit(key[i]) - m);
+  s = warp_sum_f(s);
+
+  unsigned taken = 0;
+  int my_id = 0;
+  float my_p = 0.f;
+  for (int j = 0; j < k; ++j) {
+    unsigned bk = 0, bi = 0;   // best key, and ~id (larger = lower id); 0/0 = none
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const int e = lane + 32 * i;
+      const unsigned ii = ~(unsigned)e;
+      if (e < E && !((taken >> i) & 1u) && (key[i] > bk || (key[i] == bk && ii > bi))) {
+        bk = key[i];
+        bi = ii;
+      }
+    }
+    const unsigned mk = __reduce_max_sync(kFullMask, bk);
+    const unsigned mi = __reduce_max_sync(kFullMask, bk == mk ? bi : 0u);
+    const int be = (int)~mi;
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_id = be;
+      my_p = expf(key_logit(mk) - m) / s;
+    }
+  }
+  if (renorm) {
+    const float tot = warp_sum_f(lane < k ? my_p : 0.f);
+    my_p = my_p / tot;
+  }
+  if (lane < k) {
+    ids[lane] = my_id;
+    w[lane] = my_p;
+    if (s_ids) s_ids[lane] = my_id;
+  }
+}
+
+__device__ __forceinline__ void route_dispatch(const float* row, int E, int k, int renorm,
+                                               int32_t* ids, float* w, int32_t* s_ids) {
+  if (E <= 32) route_token<1>(row, E, k, renorm, ids, w, s_ids);
+  else if (E <= 64) route_token<2>(row, E, k, renorm, ids, w, s_ids);
+  else if (E <= 128) route_token<4>(row, E, k, renorm, ids, w, s_ids);
+  else if (E <= 256) route_token<8>(row, E, k, renorm, ids, w, s_ids);
+  else if (E <= 512) route_token<16>(row, E, k, renorm, ids, w, s_ids);
+  else route_token<32>(row, E, k, renorm, ids, w, s_ids);
+}
+
+// Exclusive block-wide prefix counts of NF flags at once; s_c is [NF][33].
+// Every thread of the CTA must call it.  tot[f] gets the block totals.
+template <int NF>
+__device__ __forceinline__ void block_scan_multi(const int (&flag)[NF], int (&rank)[NF], int (&tot)[NF],
+                                                 int (*s_c)[33]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned b[NF];
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    b[f] = __ballot_sync(kFullMask, flag[f]);
+    if (lane == 0) s_c[f][warp] = __popc(b[f]);
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int f = 0; f < NF; ++f) {
+      const int v = lane < nw ? s_c[f][lane] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += t;
+      }
+      s_c[f][lane] = incl - v;
+      if (lane == 31) s_c[f][32] = incl;
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    rank[f] = s_c[f][warp] + __popc(b[f] & lt);
+    tot[f] = s_c[f][32];
+  }
+}
+
+struct PrepSmem {
+  int c[5][33];
+  int map[MOE_MAX_EXPERTS];        // expert -> slot (-1 absent)
+  int rank[MOE_MAX_EXPERTS];       // rank among the step's non-cold experts
+  int sexp[MOE_MAX_EXPERTS];       // slot -> expert (-1 free)
+  long long stamp[MOE_MAX_EXPERTS];
+  int victim[MOE_MAX_EXPERTS];
+  unsigned char mark[MOE_MAX_EXPERTS];
+  unsigned char newf[MOE_MAX_EXPERTS];   // expert copied in this step
+  unsigned char cold[MOE_MAX_EXPERTS];
+  int32_t ids[kMaxRoutedIds];
+  int bad;
+};
+
+// One layer step's bookkeeping by the calling CTA (blockDim.x >= E, a multiple
+// of 32; do_route needs T <= 64).
+__device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;   // >= E, a multiple of 32
+  const int E = a.E, N = a.N;
+  const int n_ids = a.T * a.k;
+  const bool ids_in_smem = a.do_route != 0;
+
+  // every global read the step needs, issued before anything waits
+  const unsigned long long clk = a.st->clock;
+  const int nfree = a.st->nfree;
+  if (tid < E) {
+    S.map[tid] = a.slot_map[tid];
+    S.cold[tid] = a.cold != nullptr ? a.cold[tid] : 0;
+    S.mark[tid] = 0;
+    S.newf[tid] = 0;
+  }
+  if (tid < N) {
+    S.sexp[tid] = a.slot_expert[tid];
+    S.stamp[tid] = a.slot_stamp[tid];
+  }
+  if (tid == 0) S.bad = 0;
+  if (a.do_route) {
+    for (int t = tid >> 5; t < a.T; t += nthr / 32)
+      route_dispatch(a.logits + (size_t)t * E, E, a.k, a.renorm, a.ids + (size_t)t * a.k,
+                     a.w_out + (size_t)t * a.k, S.ids + t * a.k);
+  }
+  __syncthreads();
+  for (int i = tid; i < n_ids; i += nthr) {
+    const int e = ids_in_smem ? S.ids[i] : a.ids[i];
+    if ((unsigned)e >= (unsigned)E) S.bad = 1;
+    else S.mark[e] = 1;
+  }
+  __syncthreads();
+  if (S.bad) {
+    // Reject the whole step: state untouched, every assignment skipped.
+    if (tid == 0) {
+      atomicExch(a.err, DEVERR_BAD_ID);
+      RecHdr h = {};
+      h.n_ids = n_ids;
+      *a.hdr = h;
+    }
+    for (int i = tid; i < n_ids; i += nthr) {
+      if (a.slot_ids_out) a.slot_ids_out[i] = -1;
+      if (a.asg_ptr) a.asg_ptr[i] = 0ull;
+      if (a.src_ptr) a.src_ptr[i] = 0ull;
+      if (a.pending) a.pending[i] = 0;
+    }
+    return;
+  }
+
+  const int e = tid;
+  const int sel = (e < E) ? S.mark[e] : 0;
+  const int cold = sel && S.cold[e];
+  const int nc = sel && !cold;
+  const int hit = nc && S.map[e] >= 0;
+  int flag[5] = {nc, cold, sel, hit, nc && !hit};
+  int rank[5], tot[5];
+  block_scan_multi<5>(flag, rank, tot, S.c);
+  const int D = tot[0], C = tot[1], ND = tot[2];
+  const bool bypass = D > N;
+  if (nc) {
+    a.lists[LST_NONCOLD * E + rank[0]] = e;
+    S.rank[e] = rank[0];
+    if (bypass) S.newf[e] = 1;   // bypass: every non-cold expert is copied to scratch
+  }
+  if (cold) a.lists[LST_COLD * E + rank[1]] = e;
+
+  int nh = 0, nm = 0, nvict = 0;
+  if (!bypass) {
+    const int miss = flag[4];
+    const int r_h = rank[3], r_m = rank[4];
+    nh = tot[3];
+    nm = tot[4];
+    if (hit) {
+      S.stamp[S.map[e]] = (long long)(clk + (unsigned long long)r_h);   // touch: newest stamps
+      a.lists[LST_HITS * E + r_h] = e;
+    }
+    nvict = nm > nfree ? nm - nfree : 0;
+    __syncthreads();
+    if (nvict > 0 && tid < N && S.sexp[tid] >= 0) {
+      // rank of this slot by recency among occupied slots (stamps are unique);
+      // hits were just stamped newest, so the nvict oldest are not in this step
+      const long long my = S.stamp[tid];
+      int r = 0;
+      for (int s2 = 0; s2 < N; ++s2) r += (S.sexp[s2] >= 0 && S.stamp[s2] < my);
+      if (r < nvict) S.victim[r] = tid;
+    }
+    __syncthreads();
+    int slot = -1, ev = -1;
+    if (miss) {
+      if (r_m < nfree) {
+        slot = nfree - 1 - r_m;                // free list [0, nfree), popped from the end
+      } else {
+        slot = S.victim[r_m - nfree];          // i-th least recently used slot
+        ev = S.sexp[slot];
+      }
+      a.lists[LST_MISS_E * E + r_m] = e;
+      a.lists[LST_MISS_SLOT * E + r_m] = slot;
+      a.lists[LST_MISS_EV * E + r_m] = ev;
+    }
+    __syncthreads();
+    if (miss) {
+      if (ev >= 0) S.map[ev] = -1;
+      S.newf[e] = 1;
+      S.map[e] = slot;
+      S.sexp[slot] = e;
+      S.stamp[slot] = (long long)(clk + (unsigned long long)(nh + r_m));
+    }
+  }
+  __syncthreads();
+  if (!bypass) {
+    if (e < E) a.slot_map[e] = S.map[e];
+    if (tid < N) {
+      a.slot_expert[tid] = S.sexp[tid];
+      a.slot_stamp[tid] = S.stamp[tid];
+    }
+  }
+
+  if (tid == 0) {
+    LayerState* st = a.st;
+    unsigned long long sv[ST_COUNT];
+#pragma unroll
+    for (int i = 0; i < ST_COUNT; ++i) sv[i] = st->stats[i];
+    if (n_ids > 0) sv[ST_STEPS] += 1;
+    sv[ST_COLD] += (unsigned long long)C;
+    sv[ST_B_COLD] += (unsigned long long)C * a.expert_bytes;
+    if (bypass) {
+      sv[ST_BYPASS] += 1;
+      sv[ST_B_BYPASS] += (unsigned long long)D * a.expert_bytes;
+    } else {
+      st->clock = clk + (unsigned long long)(nh + nm);
+      st->nfree = nfree - (nm < nfree ? nm : nfree);
+      sv[ST_HITS] += (unsigned long long)nh;
+      sv[ST_MISSES] += (unsigned long long)nm;
+      sv[ST_EVICT] += (unsigned long long)nvict;
+      sv[ST_B_MISS] += (unsigned long long)nm * a.expert_bytes;
+    }
+#pragma unroll
+    for (int i = 0; i < ST_COUNT; ++i) st->stats[i] = sv[i];
+    RecHdr h;
+    h.n_ids = n_ids;
+    h.bypass = bypass ? 1 : 0;
+    h.n_distinct = ND;
+    h.n_cold = C;
+    h.n_noncold = D;
+    h.n_hits = nh;
+    h.n_misses = nm;
+    h.n_evictions = nvict;
+    *a.hdr = h;
+  }
+
+  for (int i = tid; i < n_ids; i += nthr) {
+    const int x = ids_in_smem ? S.ids[i] : a.ids[i];
+    int v;
+    unsigned long long p;
+    const unsigned long long host = a.host_base + (unsigned long long)x * a.stride;
+    if (S.cold[x]) {
+      v = (int)(MOE_SLOT_COLD | (unsigned)x);
+      p = host;
+    } else if (bypass) {
+      const int r = S.rank[x];
+      v = (int)(MOE_SLOT_SCRATCH | (unsigned)r);
+      p = a.scratch_base + (unsigned long long)r * a.stride;
+    } else {
+      const int s = S.map[x];
+      v = (int)(MOE_SLOT_POOL | (unsigned)s);
+      p = a.pool_base + (unsigned long long)s * a.stride;
+    }
+    if (a.slot_ids_out) a.slot_ids_out[i] = v;
+    if (a.asg_ptr) a.asg_ptr[i] = p;
+    if (a.src_ptr) a.src_ptr[i] = host;
+    if (a.pending) a.pending[i] = S.newf[x];
+  }
+}
+
+
+}  // namespace prep
+}  // namespace moe

@@ -328,10 +328,19 @@ moe_status moe_cache_check(moe_cache_t* c);
 /* Empty every pool, zero the counters and the device error flag. */
 moe_status moe_cache_reset(moe_cache_t* c);
 
-/* Per-phase event timing: on != 0 starts (and clears) accumulation. */
-moe_status moe_cache_set_timing(moe_cache_t* c, int on);
+/* Per-phase event timing: on != 0 starts (and clears) accumulation; capacity
+ * = launches per phase to reserve events for (0 = 4096).  Reserve enough
+ * before a stream capture: no events are created while capturing, and
+ * launches past the reserve go untimed. */
+moe_status moe_cache_set_timing(moe_cache_t* c, int on, int capacity);
 /* Synchronises the device and returns the accumulated per-phase times. */
 moe_status moe_cache_read_timing(moe_cache_t* c, moe_cache_timing* out);
+/* Per-launch record of the expert-MLP phase (synchronises): ms_h[i] = GPU
+ * time of the i-th timed MLP launch, misses_h[i] = misses of that layer step
+ * (copied on the device, so it is right under graph replay too).  Up to `cap`
+ * records; *n receives the number available. */
+moe_status moe_cache_read_timing_launches(moe_cache_t* c, float* ms_h, int32_t* misses_h, int cap,
+                                          int* n);
 
 #ifdef __cplusplus
 }
