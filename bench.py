@@ -408,7 +408,7 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded Zipf routing with reuse; N(0,0.02) weights)",
             "config": {"workload": workload_desc(w), "tokens_per_step": w.tokens,
-                       "copy_mode": info["copy_mode_name"], "graph": graph is not None,
+                       "copy_mode": info["copy_mode_name"], "graph": use_graph,
                        "l2": "inputs larger than L2: every step reads "
                              f"{w.layers * w.top_k * lay['total'] / 1e9:.2f} GB of expert weights",
                        "parallelism": f"replicas x{world}"},
@@ -437,7 +437,6 @@ def run_ours(args, w):
                                     "sample": f"{cpu_n} (token, layer) steps of the first 2 decode tokens "
                                               f"in {cpu_dt:.1f} s (float64 numpy, BLAS threads as installed)"}
         print(json.dumps(line), flush=True)
-    del graph
     c.close()
     if world > 1:
         import torch.distributed as dist

@@ -23,6 +23,8 @@ MOE_COPY_AUTO, MOE_COPY_MEMCPY, MOE_COPY_UVA, MOE_COPY_FUSED = 0, 1, 2, 3
 COPY_MODE = {"auto": MOE_COPY_AUTO, "memcpy": MOE_COPY_MEMCPY, "uva": MOE_COPY_UVA,
              "fused": MOE_COPY_FUSED}
 COPY_MODE_NAME = {v: k for k, v in COPY_MODE.items()}
+MOE_MLP_AUTO, MOE_MLP_PLAIN = 0, 1
+MLP_KERNEL = {"auto": MOE_MLP_AUTO, "plain": MOE_MLP_PLAIN}
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ETIMEOUT, MOE_ESTATE = 0, -1, -2, -3, -4, -5
 STATUS_NAME = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ENOMEM", -3: "MOE_ECUDA",
                -4: "MOE_ETIMEOUT", -5: "MOE_ESTATE"}
@@ -36,7 +38,7 @@ class moe_cache_config(C.Structure):
                 ("hidden", C.c_int), ("inter", C.c_int), ("wdtype", C.c_int),
                 ("slots_per_layer", C.c_int), ("max_tokens", C.c_int), ("renormalize", C.c_int),
                 ("cold_mask_h", C.POINTER(C.c_uint8)), ("copy_mode", C.c_int), ("device", C.c_int),
-                ("hbm_budget_bytes", C.c_size_t)]
+                ("hbm_budget_bytes", C.c_size_t), ("mlp_kernel", C.c_int)]
 
 
 class moe_cache_counters(C.Structure):
@@ -177,7 +179,8 @@ class MoECache:
     """One library handle: L layers of E experts with N pool slots each."""
 
     def __init__(self, num_layers, num_experts, top_k, hidden, inter, wdtype, slots, max_tokens,
-                 renormalize=False, cold_mask=None, copy_mode="uva", device=0, hbm_budget_bytes=0):
+                 renormalize=False, cold_mask=None, copy_mode="uva", device=0, hbm_budget_bytes=0,
+                 mlp_kernel="auto"):
         self.L, self.E, self.k, self.H, self.I = num_layers, num_experts, top_k, hidden, inter
         self.wdtype, self.N, self.max_tokens = wdtype, slots, max_tokens
         cfg = moe_cache_config()
@@ -193,6 +196,7 @@ class MoECache:
         cfg.copy_mode = COPY_MODE[copy_mode]
         cfg.device = device
         cfg.hbm_budget_bytes = hbm_budget_bytes
+        cfg.mlp_kernel = MLP_KERNEL[mlp_kernel]
         h = _H()
         _check(lib().moe_cache_create(C.byref(cfg), C.byref(h)))
         self._h = h

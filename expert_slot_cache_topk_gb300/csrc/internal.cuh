@@ -35,7 +35,7 @@ struct RecHdr {
 enum { LST_HITS = 0, LST_MISS_E, LST_MISS_SLOT, LST_MISS_EV, LST_COLD, LST_NONCOLD, LST_COUNT };
 
 // Device error flag values (sticky until reset)
-enum { DEVERR_NONE = 0, DEVERR_BAD_ID = 1, DEVERR_BARRIER = 2 };
+enum { DEVERR_NONE = 0, DEVERR_BAD_ID = 1, DEVERR_BARRIER = 2, DEVERR_RING = 3 };
 
 // Grid-wide barrier state of the fused MLP kernel (count returns to 0 after
 // every barrier; gen counts completed barriers).
@@ -104,12 +104,17 @@ struct MlpArgs {
   const unsigned long long* src_ptr;
   int readthrough;
   unsigned long long tail_off, tail_bytes;
+  // Device addresses [host_lo, host_hi) are the mapped pinned backing store:
+  // the staged decode kernel reads blocks there with plain loads, never with
+  // bulk copies (0, 0 = no host blocks).
+  unsigned long long host_lo, host_hi;
 };
 
 // ---- launchers (k_route_prepare.cu) ----
 cudaError_t launch_router(const float* logits, int T, int E, int k, int renorm,
                           int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s);
+cudaError_t prepare_configure();   // kernel attributes, call outside capture
 cudaError_t launch_copy(const CopyArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_copy_raw(const void* src, void* dst, unsigned long long nvec, int grid,
                             cudaStream_t s);
@@ -128,5 +133,27 @@ cudaError_t launch_mlp_down(int wdtype, const MlpArgs& a, cudaStream_t s);
 cudaError_t launch_mlp_fused(int wdtype, const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s);
 size_t mlp_down_smem_bytes(int k, int I);
 size_t mlp_up_smem_bytes(int H);
+
+// ---- launchers (k_mlp_ring.cu): one-token expert MLP with weights staged in
+// shared memory by bulk copies; cudaErrorNotSupported = use launch_mlp_fused.
+cudaError_t mlp_ring_configure(int wdtype, int H, int I, int k);  // call outside capture
+cudaError_t launch_mlp_ring(int wdtype, const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s);
+
+// ---- launchers (k_moe_gemm.cu): grouped expert MLP on the tensor cores for
+// steps with several tokens (group by expert, tcgen05 up and down GEMMs,
+// combine).  cudaErrorNotSupported = use the per-token kernels.
+struct GemmBuffers {
+  const int32_t* ids;      // [T*k] routed expert ids
+  int E;
+  int32_t* order;          // [T*k]
+  int4* tiles;             // [T*k]
+  int* ntiles;             // [1]
+  uint16_t* hb;            // [T*k, I] bf16
+  float* out;              // [T*k, H] f32
+  int* err;
+};
+bool moe_gemm_supported(int wdtype, int H, int I, int k);
+cudaError_t moe_gemm_configure(int wdtype);   // call outside capture
+cudaError_t launch_moe_gemm(int wdtype, const MlpArgs& a, const GemmBuffers& b, cudaStream_t s);
 
 }  // namespace moe

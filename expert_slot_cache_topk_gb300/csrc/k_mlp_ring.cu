@@ -1,0 +1,867 @@
+// One-token (decode) expert MLP with the weight bytes staged in shared memory.
+//
+// Same arithmetic as k_mlp.cu -- up: h[j, i] = w_j * silu(Wg_j[i] . x) *
+// (Wu_j[i] . x); down: y[n] = sum over the k experts' concatenated W2 rows
+// n . h -- but organised for a batch-1 step, where every weight byte is used
+// once and the step is a stream of k * B_e bytes out of HBM (vLLM PR #37190
+// "Run MoE models exceeding VRAM via expert CPU offloading with GPU cache",
+// "How it works": the experts run on slot buffers through remapped ids).
+//
+// One persistent CTA per SM, cooperative launch, nine warps:
+//   * warp 0 (producer) walks this CTA's share of the work -- first its run
+//     of gate/up row pairs (expert-major), then its output rows -- and for
+//     every stage issues cp.async.bulk copies of the weight rows that live in
+//     HBM into a ring of shared-memory stages, signalled by mbarriers;
+//   * warps 1..8 (consumers) take every stage in order: up stages produce h,
+//     then all CTAs meet at a grid barrier (h complete), then down stages
+//     produce y.  The producer never waits for the grid barrier, so W2 rows
+//     keep streaming into the ring while the grid synchronises.
+// Rows of blocks in mapped host memory (cold experts; missed experts read
+// through in the same step, "Running 125B MoE on Two 32 GB Cards", section 2:
+// the GPU reads host rows through a UVA view) are not bulk-copied: the
+// consumers read them with plain 16-byte loads, and a read-through row is
+// also stored into the expert's slot.
+//
+// The consumer warps keep the token's activations in registers (x in the up
+// phase, one part of h in the down phase; see RingTile), so shared memory
+// carries only weight bytes.  Each output is reduced in a fixed order that
+// does not depend on where an expert's bytes live, so pool, scratch and host
+// homes give bitwise identical y; the order differs from k_mlp.cu's, so the
+// two kernels agree to rounding, not bitwise.
+//
+// Ring protocol: stage s of the ring holds work item i with i % NS == s.
+// full[s] completes once per item (producer arrive + the bulk bytes),
+// empty[s] once per item (one arrive per consumer warp).  Every consumer warp
+// takes every item in order, so no waiter is ever more than one phase ahead
+// of a barrier.  Waits are bounded by the global timer; a wait that runs out
+// sets DEVERR_RING and the CTA stops, after the producer has waited (bounded)
+// for its own copies in flight.
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "internal.cuh"
+#include "mlp_common.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace mlp;
+
+constexpr int kConsumers = 8;                       // consumer warps
+constexpr int kRingThreads = 32 * (1 + kConsumers);
+constexpr int kMaxStages = 12;
+constexpr int kMaxRows = 64;                        // output rows per CTA whose residual is kept in shared memory
+constexpr int kParts = 4;                           // parts per output row in the down phase
+constexpr int kRowsPerPass = kConsumers / kParts;   // output rows the consumer warps take at once
+constexpr int kBatch = 8;                           // chunks per lane in flight on the plain-load paths
+constexpr unsigned long long kWaitNs = 500000000ull;  // 0.5 s
+constexpr size_t kSmemLimit = 227 * 1024;
+
+enum { SRC_RING = 0, SRC_PLAIN = 1, SRC_NONE = 2 };
+
+struct RingDesc {
+  int kind;        // 0 = up, 1 = down
+  int asg;         // up: assignment index
+  int p0;          // up: first row pair; down: first output row
+  int n;           // up: pairs; down: rows
+  unsigned src;    // up: SRC_*; down: bit j set = expert j not in the ring
+};
+
+struct RingShared {
+  unsigned long long full[kMaxStages];
+  unsigned long long empty[kMaxStages];
+  RingDesc desc[kMaxStages];
+  unsigned long long base[MOE_MAX_TOPK];   // block pointer of each assignment
+  float wt[MOE_MAX_TOPK];                  // router weight of each assignment
+  float xres[kMaxRows];                    // residual x of this CTA's output rows
+  float part[2][kParts * kConsumers];      // down: the part sums of each row, by item parity
+  float gu[kMaxStages][kConsumers / 2][2]; // up, half-size items: gate / up sums of each pair
+  int cnt[kMaxStages][kConsumers / 2];     // up, half-size items: rows of the pair finished
+  int stop;                                // set when a wait ran out: skip the rest
+  unsigned long long hbar;                 // the bulk copy of h has landed
+};
+
+struct RingCfg {
+  int up_pairs;           // row pairs per up item: kConsumers or kConsumers / 2
+  int nstages;            // ring stages
+  unsigned stage_bytes;   // bytes per stage (multiple of 128)
+  int down_rows;          // output rows per down item (<= kConsumers)
+  int down_group;         // CTA row ranges start at multiples of this (8 for INT4 scale rows)
+  unsigned h_off;         // byte offset of the h copy (k * I f32) after the ring stages
+};
+
+// ------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, unsigned parity) {
+  unsigned ok;
+  asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+               : "=r"(ok)
+               : "r"(bar), "r"(parity)
+               : "memory");
+  return ok != 0;
+}
+// true once the phase with this parity has completed; false after kWaitNs
+// (the clock is read only when the first try finds the phase still open)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    if (mbar_try(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+}
+// bytes (multiple of 16) from global src (16-byte aligned) to shared dst
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, unsigned bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
+}
+
+__device__ __forceinline__ bool in_host(const MlpArgs& a, unsigned long long p) {
+  return p >= a.host_lo && p < a.host_hi;
+}
+
+// Grid barrier among the consumer warps of every CTA (the producer warps do
+// not take part).  The CTA's writes are ordered before the arrival by the
+// CTA barrier plus one thread's fence (fences are cumulative); that thread
+// polls the generation word with acquire loads.  Bounded: gives up after
+// ~1 s and flags DEVERR_BARRIER.
+__device__ __forceinline__ void consumer_grid_barrier(GridBar* bar, int* err, int ctid) {
+  // h written here is read by another CTA's bulk copy (async proxy)
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  consumer_sync();
+  if (ctid == 0) {
+    const unsigned gen = *reinterpret_cast<volatile unsigned*>(&bar->gen);
+    __threadfence();
+    const unsigned arrived = atomicAdd(&bar->count, 1u);
+    if (arrived == gridDim.x - 1) {
+      atomicExch(&bar->count, 0u);
+      __threadfence();
+      atomicAdd(&bar->gen, 1u);
+    } else {
+      const unsigned long long t0 = global_ns();
+      for (unsigned it = 0;; ++it) {
+        unsigned g;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(&bar->gen) : "memory");
+        if (g != gen) break;
+        if ((it & 255u) == 255u && global_ns() - t0 > 1000000000ull) {
+          atomicExch(err, DEVERR_BARRIER);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  consumer_sync();
+}
+
+// x[0, n] as f32, and y[0, n] = v (bf16 unless F is f32)
+template <int F>
+__device__ __forceinline__ float x_at(const MlpArgs& a, int n) {
+  return F == MOE_F32 ? reinterpret_cast<const float*>(a.x)[n] : bf16_bits(reinterpret_cast<const uint16_t*>(a.x)[n]);
+}
+template <int F>
+__device__ __forceinline__ void store_out(const MlpArgs& a, int n, float v) {
+  if (F == MOE_F32) reinterpret_cast<float*>(a.y)[n] = v;
+  else reinterpret_cast<__nv_bfloat16*>(a.y)[n] = __float2bfloat16_rn(v);
+}
+
+// ------------------------------------------------------------- consumers
+// Per-format register tiling of the consumer warps.  Lane l owns the 16-byte
+// chunks c = l + 32 m (m < XM) of every w13 row and keeps the matching x
+// values in registers for the whole up phase.  In the down phase every
+// output row is cut into kParts parts of Qp = ceil(Q / kParts) chunks of the
+// k experts' concatenated W2 rows (Q chunks); warp w owns part w % kParts of
+// its rows -- chunks q = part * Qp + l + 32 m (m < HM) -- and keeps those h
+// values in registers.  Shared memory then only carries the weight bytes.
+template <int F>
+struct RingTile;
+template <>
+struct RingTile<MOE_F32> {
+  static constexpr int XM = 8, HM = 8;
+};
+template <>
+struct RingTile<MOE_BF16> {
+  static constexpr int XM = 8, HM = 8;
+};
+template <>
+struct RingTile<MOE_INT4_G128> {
+  static constexpr int XM = 3, HM = 2;
+};
+
+// dot product of one 16-byte weight chunk with EL activations in registers
+template <int F>
+__device__ __forceinline__ float chunk_dot_r(const uint4 w, const float* x) {
+  return chunk_dot<F>(w, x);
+}
+
+// activation chunk (EL values) -> registers; x is bf16 unless F is f32
+template <int F>
+__device__ __forceinline__ void load_x_chunk(float* dst, const void* x, int c) {
+  constexpr int EL = FmtT<F>::kElems;
+  if (F == MOE_F32) {
+    const float4 v = reinterpret_cast<const float4*>(x)[c];
+    dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < EL / 8; ++i) {
+      const uint4 v = reinterpret_cast<const uint4*>(x)[(size_t)c * (EL / 8) + i];
+      float* d = dst + 8 * i;
+      d[0] = bf16_lo(v.x); d[1] = bf16_hi(v.x); d[2] = bf16_lo(v.y); d[3] = bf16_hi(v.y);
+      d[4] = bf16_lo(v.z); d[5] = bf16_hi(v.z); d[6] = bf16_lo(v.w); d[7] = bf16_hi(v.w);
+    }
+  }
+}
+
+// Dot products of NR weight rows with the token's x (registers), reduced
+// over the warp; every lane gets the sums.  Row r's 16-byte chunks come from
+// the stage (ring) or from global memory (plain loads; with `copy`, also
+// stored to cpy[r], the row's place in the expert's slot).  INT4 scales come
+// from srow[r] (bf16, one per 128 elements).
+template <int F, int NR>
+__device__ __forceinline__ void rows_dot(const uint4* const (&row)[NR], const uint16_t* const (&srow)[NR],
+                                         uint4* const (&cpy)[NR], bool ring, bool copy, int C,
+                                         const float (&xr)[RingTile<F>::XM][FmtT<F>::kElems], int lane,
+                                         float (&out)[NR]) {
+  constexpr int XM = RingTile<F>::XM;
+  uint4 wv[NR][XM];
+  float sc[NR][XM];
+#pragma unroll
+  for (int m = 0; m < XM; ++m) {
+    const int c = lane + 32 * m;
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      wv[r][m] = make_uint4(0u, 0u, 0u, 0u);
+      sc[r][m] = 0.f;
+      if (c < C) {
+        wv[r][m] = ring ? row[r][c] : __ldcs(row[r] + c);
+        if (F == MOE_INT4_G128) sc[r][m] = bf16_bits(srow[r][c >> 2]);
+      }
+    }
+  }
+  if (copy) {
+#pragma unroll
+    for (int m = 0; m < XM; ++m) {
+      const int c = lane + 32 * m;
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+        if (c < C) cpy[r][c] = wv[r][m];
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float acc = 0.f;
+#pragma unroll
+    for (int m = 0; m < XM; ++m) {
+      const float dd = chunk_dot_r<F>(wv[r][m], xr[m]);
+      acc = (F == MOE_INT4_G128) ? fmaf(dd, sc[r][m], acc) : acc + dd;
+    }
+    out[r] = warp_sum(acc);
+  }
+}
+
+__device__ __forceinline__ float swiglu_h(const RingShared& S, unsigned long long base, int asg, float g, float u) {
+  return base != 0ull ? S.wt[asg] * (g / (1.0f + expf(-g)) * u) : 0.f;
+}
+
+// Up item of P = d.n row pairs (pairs d.p0 .. d.p0 + P - 1 of assignment
+// d.asg).  The stage holds [gate rows (P) | up rows (P) | gate scales (P) |
+// up scales (P)], so stage row r is gate row p0 + r for r < P, else up row
+// I + p0 + r - P.
+//   P == kConsumers: warp cw takes pair cw, both of its rows.
+//   P == kConsumers / 2: warp cw takes stage row cw alone; the two warps of a
+//   pair meet through S.gu / S.cnt of this stage (the second one to finish
+//   writes h), so no barrier is needed.
+template <int F>
+__device__ __forceinline__ void up_item(const MlpArgs& a, RingShared& S, const RingDesc& d, int s,
+                                        const uint8_t* stage, const float (&xr)[RingTile<F>::XM][FmtT<F>::kElems],
+                                        int cw, int lane) {
+  const int P = d.n;
+  const int C = a.H / FmtT<F>::kElems;
+  const int G = a.H / 128;
+  const size_t rb = row_bytes<F>(a.H);
+  const unsigned long long base = S.base[d.asg];
+  const bool ring = d.src == SRC_RING;
+  const bool copy = d.src == SRC_PLAIN && a.readthrough && a.pending[d.asg] != 0;
+  const unsigned long long blk = copy ? a.src_ptr[d.asg] : base;
+  // stage row r -> weight row of the expert block
+  auto wrow = [&](int r) { return r < P ? d.p0 + r : a.I + d.p0 + r - P; };
+  auto rowp = [&](int r) -> const uint4* {
+    return ring ? reinterpret_cast<const uint4*>(stage + (size_t)r * rb)
+                : reinterpret_cast<const uint4*>(blk + (size_t)wrow(r) * rb);
+  };
+  auto srowp = [&](int r) -> const uint16_t* {
+    return ring ? reinterpret_cast<const uint16_t*>(stage + 2 * (size_t)P * rb) + (size_t)r * G
+                : reinterpret_cast<const uint16_t*>(blk + a.off_s13) + (size_t)wrow(r) * G;
+  };
+  auto cpyp = [&](int r) { return reinterpret_cast<uint4*>(base + (size_t)wrow(r) * rb); };
+  if (P == kConsumers) {
+    float v[2] = {0.f, 0.f};
+    if (d.src != SRC_NONE) {
+      const uint4* const rows[2] = {rowp(cw), rowp(P + cw)};
+      const uint16_t* const srows[2] = {srowp(cw), srowp(P + cw)};
+      uint4* const cpys[2] = {copy ? cpyp(cw) : nullptr, copy ? cpyp(P + cw) : nullptr};
+      rows_dot<F, 2>(rows, srows, cpys, ring, copy, C, xr, lane, v);
+    }
+    if (lane == 0) a.h[(size_t)d.asg * a.I + d.p0 + cw] = swiglu_h(S, base, d.asg, v[0], v[1]);
+  } else {
+    float v[1] = {0.f};
+    if (d.src != SRC_NONE) {
+      const uint4* const rows[1] = {rowp(cw)};
+      const uint16_t* const srows[1] = {srowp(cw)};
+      uint4* const cpys[1] = {copy ? cpyp(cw) : nullptr};
+      rows_dot<F, 1>(rows, srows, cpys, ring, copy, C, xr, lane, v);
+    }
+    if (lane == 0) {
+      const int pr = cw % P, role = cw / P;   // role 0 = gate, 1 = up
+      S.gu[s][pr][role] = v[0];
+      __threadfence_block();
+      if (atomicAdd(&S.cnt[s][pr], 1) == 1) {
+        __threadfence_block();
+        const float g = S.gu[s][pr][0], u = S.gu[s][pr][1];
+        S.cnt[s][pr] = 0;
+        a.h[(size_t)d.asg * a.I + d.p0 + pr] = swiglu_h(S, base, d.asg, g, u);
+      }
+    }
+  }
+}
+
+// Down item: output rows d.p0 + r, r < d.n.  Consumer warp cw takes part
+// cw % kParts of rows r = cw / kParts + kRowsPerPass i, two rows at a time
+// (independent accumulators, one chunk decode for both).  The stage holds,
+// per expert j in the ring, its d.n W2 rows at j * d.n * rb2, then (INT4) its
+// scale rows after all the weight rows.  qj[m] packs (expert << 16 | chunk in
+// expert row) of this lane's chunk m, or -1.
+template <int F>
+__device__ __forceinline__ void down_rows(const MlpArgs& a, const RingShared& S, const RingDesc& d,
+                                          const uint8_t* stage, const float (&hr)[RingTile<F>::HM][FmtT<F>::kElems],
+                                          const int (&qj)[RingTile<F>::HM], float* part, int cw, int lane) {
+  constexpr int HM = RingTile<F>::HM;
+  const int G2 = a.I / 128;
+  const size_t rb2 = row_bytes<F>(a.I);
+  const size_t wbytes = (size_t)d.n * rb2;
+  const size_t sbytes = (size_t)d.n * G2 * 2;
+  const uint8_t* sring = stage + (size_t)a.k * wbytes;
+  // per chunk: byte offset of row 0 in the stage (or -1: not in the ring)
+  uint32_t off[HM], soff[HM];
+#pragma unroll
+  for (int m = 0; m < HM; ++m) {
+    const int e = qj[m];
+    off[m] = 0xffffffffu;
+    soff[m] = 0u;
+    if (e >= 0) {
+      const int j = e >> 16, c = e & 0xffff;
+      if (S.base[j] != 0ull && !((d.src >> j) & 1u)) {
+        off[m] = (uint32_t)((size_t)j * wbytes + (size_t)c * 16);
+        soff[m] = (uint32_t)((size_t)j * sbytes + (size_t)(c >> 2) * 2);
+      }
+    }
+  }
+  for (int r0 = cw / kParts; r0 < d.n; r0 += 2 * kRowsPerPass) {
+    const int r1 = r0 + kRowsPerPass;
+    const bool two = r1 < d.n;
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int m = 0; m < HM; ++m) {
+      uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+      float s0 = 0.f, s1 = 0.f;
+      if (off[m] != 0xffffffffu) {
+        w0 = *reinterpret_cast<const uint4*>(stage + off[m] + (size_t)r0 * rb2);
+        if (two) w1 = *reinterpret_cast<const uint4*>(stage + off[m] + (size_t)r1 * rb2);
+        if (F == MOE_INT4_G128) {
+          const uint16_t* sp = reinterpret_cast<const uint16_t*>(sring + soff[m]);
+          s0 = bf16_bits(sp[(size_t)r0 * G2]);
+          if (two) s1 = bf16_bits(sp[(size_t)r1 * G2]);
+        }
+      } else if (qj[m] >= 0) {
+        // expert read from global memory: missing, host-resident or read through
+        const int j = qj[m] >> 16, c = qj[m] & 0xffff;
+        const unsigned long long blk = S.base[j];
+        if (blk != 0ull) {
+          const uint4* wrow = reinterpret_cast<const uint4*>(blk + a.off_w2) + c;
+          const unsigned short* srow = reinterpret_cast<const unsigned short*>(blk + a.off_s2) + (c >> 2);
+          const size_t n0 = (size_t)(d.p0 + r0), n1 = (size_t)(d.p0 + r1);
+          w0 = __ldcg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(wrow) + n0 * rb2));
+          if (two) w1 = __ldcg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(wrow) + n1 * rb2));
+          if (F == MOE_INT4_G128) {
+            s0 = bf16_bits(__ldcg(srow + n0 * G2));
+            if (two) s1 = bf16_bits(__ldcg(srow + n1 * G2));
+          }
+        }
+      }
+      const float d0 = chunk_dot_r<F>(w0, hr[m]);
+      const float d1 = chunk_dot_r<F>(w1, hr[m]);
+      if (F == MOE_INT4_G128) {
+        acc0 = fmaf(d0, s0, acc0);
+        acc1 = fmaf(d1, s1, acc1);
+      } else {
+        acc0 += d0;
+        acc1 += d1;
+      }
+    }
+    acc0 = warp_sum(acc0);
+    acc1 = warp_sum(acc1);
+    if (lane == 0) {
+      part[kParts * r0 + cw % kParts] = acc0;
+      if (two) part[kParts * r1 + cw % kParts] = acc1;
+    }
+  }
+}
+
+// ------------------------------------------------------------- producer
+// Items of CTA b of G: up items = groups of P = up_pairs consecutive row
+// pairs of one assignment, groups [b*NG/G, (b+1)*NG/G) of NG = k * I / P
+// (expert-major); then down items = runs of down_rows output rows of the
+// CTA's row range (whole groups of down_group rows).
+struct Share {
+  int g_beg, g_end;   // up groups
+  int n0, n1;         // output rows
+  int n_up, n_items;
+};
+
+__device__ __forceinline__ Share cta_share(const MlpArgs& a, const RingCfg& rc) {
+  Share w;
+  const long long G = gridDim.x, b = blockIdx.x;
+  const long long ng = (long long)a.k * (a.I / rc.up_pairs);
+  w.g_beg = (int)(ng * b / G);
+  w.g_end = (int)(ng * (b + 1) / G);
+  const long long nrg = a.H / rc.down_group;
+  w.n0 = (int)(nrg * b / G) * rc.down_group;
+  w.n1 = (int)(nrg * (b + 1) / G) * rc.down_group;
+  w.n_up = w.g_end - w.g_beg;
+  w.n_items = w.n_up + (w.n1 - w.n0 + rc.down_rows - 1) / rc.down_rows;
+  return w;
+}
+
+template <int F>
+__device__ __forceinline__ void produce(const MlpArgs& a, const RingCfg& rc, RingShared& S, uint8_t* ring,
+                                        int lane, int* err) {
+  const Share w = cta_share(a, rc);
+  const int NS = rc.nstages;
+  const size_t rb1 = row_bytes<F>(a.H), rb2 = row_bytes<F>(a.I);
+  const size_t srb1 = F == MOE_INT4_G128 ? (size_t)(a.H / 128) * 2 : 0;
+  const size_t srb2 = F == MOE_INT4_G128 ? (size_t)(a.I / 128) * 2 : 0;
+  const int P = rc.up_pairs;
+  const int gpe = a.I / P;   // groups per expert
+  // experts that are not bulk-copied: no block, host blocks, blocks filled by
+  // read-through in this step, or (defensively) blocks not 16-byte aligned
+  const unsigned long long myb = lane < a.k ? S.base[lane] : 0ull;
+  const bool plain = lane < a.k && (myb == 0ull || in_host(a, myb) || (myb & 15ull) != 0ull ||
+                                    (a.readthrough && a.pending[lane] != 0));
+  const unsigned plain_mask = __ballot_sync(kFull, plain);
+  const unsigned k_mask = a.k >= 32 ? kFull : ((1u << a.k) - 1u);
+  const int n_ring = __popc(k_mask & ~plain_mask);
+  int i = 0;
+  for (; i < w.n_items; ++i) {
+    const int s = i % NS;
+    const uint32_t full = smem_u32(&S.full[s]);
+    uint8_t* st = ring + (size_t)s * rc.stage_bytes;
+    bool ok = true;
+    if (lane == 0 && i >= NS) ok = mbar_wait(smem_u32(&S.empty[s]), (unsigned)((i / NS) - 1) & 1u);
+    ok = __shfl_sync(kFull, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        atomicExch(err, DEVERR_RING);
+        *reinterpret_cast<volatile int*>(&S.stop) = 1;
+      }
+      break;
+    }
+    if (i < w.n_up) {
+      const int gg = w.g_beg + i;
+      const int j = gg / gpe;
+      const int p0 = (gg - j * gpe) * P;
+      const unsigned long long blk = __shfl_sync(kFull, myb, j);
+      const bool pl = (plain_mask >> j) & 1u;
+      const unsigned src = blk == 0ull ? SRC_NONE : (pl ? SRC_PLAIN : SRC_RING);
+      if (lane == 0) S.desc[s] = RingDesc{0, j, p0, P, src};
+      if (src == SRC_RING) {
+        const unsigned wb = (unsigned)(P * rb1), sb = (unsigned)(P * srb1);
+        if (lane == 0) mbar_arrive_tx(full, 2u * (wb + sb));
+        __syncwarp();
+        const uint8_t* w13 = reinterpret_cast<const uint8_t*>(blk);
+        if (lane == 0) bulk_copy(smem_u32(st), w13 + (size_t)p0 * rb1, wb, full);
+        if (lane == 1) bulk_copy(smem_u32(st + wb), w13 + (size_t)(a.I + p0) * rb1, wb, full);
+        if (sb != 0u) {
+          const uint8_t* s13 = w13 + a.off_s13;
+          if (lane == 2) bulk_copy(smem_u32(st + 2 * wb), s13 + (size_t)p0 * srb1, sb, full);
+          if (lane == 3) bulk_copy(smem_u32(st + 2 * wb + sb), s13 + (size_t)(a.I + p0) * srb1, sb, full);
+        }
+      } else if (lane == 0) {
+        mbar_arrive(full);
+      }
+    } else {
+      const int n = w.n0 + (i - w.n_up) * rc.down_rows;
+      const int nr = min(rc.down_rows, w.n1 - n);
+      if (lane == 0) S.desc[s] = RingDesc{1, 0, n, nr, plain_mask};
+      const unsigned wb = (unsigned)(nr * rb2), sb = (unsigned)(nr * srb2);
+      const unsigned bytes = (unsigned)n_ring * (wb + sb);
+      if (lane == 0) {
+        if (bytes) mbar_arrive_tx(full, bytes);
+        else mbar_arrive(full);
+      }
+      __syncwarp();
+      if (lane < a.k && !plain) {
+        const uint8_t* blk = reinterpret_cast<const uint8_t*>(myb);
+        bulk_copy(smem_u32(st + (size_t)lane * wb), blk + a.off_w2 + (size_t)n * rb2, wb, full);
+        if (sb != 0u)
+          bulk_copy(smem_u32(st + (size_t)a.k * wb + (size_t)lane * sb), blk + a.off_s2 + (size_t)n * srb2, sb,
+                    full);
+      }
+    }
+  }
+  // every copy this CTA issued has landed before it may exit
+  if (lane == 0) {
+    for (int q = i > NS ? i - NS : 0; q < i; ++q)
+      if (!mbar_wait(smem_u32(&S.full[q % NS]), (unsigned)(q / NS) & 1u)) atomicExch(err, DEVERR_RING);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------- consumer driver
+template <int F>
+__device__ __forceinline__ void consume(const MlpArgs& a, const RingCfg& rc, RingShared& S, const uint8_t* ring,
+                                        GridBar* bar, int* err, int cw, int lane) {
+  constexpr int EL = FmtT<F>::kElems;
+  constexpr int XM = RingTile<F>::XM, HM = RingTile<F>::HM;
+  const Share w = cta_share(a, rc);
+  const int NS = rc.nstages;
+  const int ctid = cw * 32 + lane;
+  volatile int* stop = &S.stop;
+  // read-through: this CTA's share of the copies of the missed experts' bytes
+  // after w13 (w2 and scales) into their slots, 4 KiB per task; they complete
+  // before the grid barrier, so the down items may read them from the slots
+  if (a.readthrough) {
+    const unsigned pend = __ballot_sync(kFull, lane < a.k && a.pending[lane] != 0 && S.base[lane] != 0ull);
+    if (pend) {
+      const unsigned long long cpe = (a.tail_bytes + 4095ull) / 4096ull;
+      const unsigned long long ncopy = (unsigned long long)__popc(pend) * cpe;
+      const unsigned long long c_beg = ncopy * blockIdx.x / gridDim.x;
+      const unsigned long long c_end = ncopy * (blockIdx.x + 1) / gridDim.x;
+      for (unsigned long long c = c_beg + cw; c < c_end; c += kConsumers) {
+        const int sidx = (int)(c / cpe);
+        const unsigned long long off = a.tail_off + (c - (unsigned long long)sidx * cpe) * 4096ull;
+        const int asg = nth_set_bit(pend, sidx);
+        const uint4* src = reinterpret_cast<const uint4*>(a.src_ptr[asg] + off);
+        uint4* dst = reinterpret_cast<uint4*>(S.base[asg] + off);
+        const unsigned long long nv = (a.tail_off + a.tail_bytes - off) / 16ull;
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const unsigned q = lane + 32u * u;
+          if (q < nv) v[u] = __ldcs(src + q);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const unsigned q = lane + 32u * u;
+          if (q < nv) dst[q] = v[u];
+        }
+      }
+    }
+  }
+  bool dead = false;
+  int i = 0;
+  // ---- up items: x of the token in registers
+  {
+    float xr[XM][EL];
+    const int C = a.H / EL;
+#pragma unroll
+    for (int m = 0; m < XM; ++m) {
+      const int c = lane + 32 * m;
+      if (c < C) {
+        load_x_chunk<F>(xr[m], a.x, c);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EL; ++e) xr[m][e] = 0.f;
+      }
+    }
+    for (; i < w.n_up; ++i) {
+      const int s = i % NS;
+      if (!dead && *stop) dead = true;
+      if (!dead) {
+        const bool ok = mbar_wait(smem_u32(&S.full[s]), (unsigned)(i / NS) & 1u);
+        if (!__all_sync(kFull, ok)) {
+          dead = true;
+          if (lane == 0) {
+            atomicExch(err, DEVERR_RING);
+            *stop = 1;
+          }
+        }
+      }
+      if (!dead) {
+        const RingDesc d = S.desc[s];
+        if (cw < 2 * d.n) up_item<F>(a, S, d, s, ring + (size_t)s * rc.stage_bytes, xr, cw, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
+    }
+  }
+  // h complete everywhere; W2 rows keep landing in the ring meanwhile
+  consumer_grid_barrier(bar, err, ctid);
+  if (i >= w.n_items) return;
+  // ---- down items: this warp's half of h in registers
+  {
+    const int C2 = a.I / EL;
+    const int Q = a.k * C2;
+    const int Qp = (Q + kParts - 1) / kParts;
+    const int pt = cw % kParts;
+    const int q_end = min(Q, (pt + 1) * Qp);
+    // h (k * I f32) -> shared memory in one bulk copy, then this warp's part
+    // of it -> registers
+    const float* hs = reinterpret_cast<const float*>(ring + rc.h_off);
+    const unsigned hbytes = (unsigned)(a.k * a.I * 4);
+    if (ctid == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_arrive_tx(smem_u32(&S.hbar), hbytes);
+      for (unsigned o = 0; o < hbytes; o += 16384u)
+        bulk_copy(smem_u32(ring + rc.h_off + o), reinterpret_cast<const uint8_t*>(a.h) + o,
+                  hbytes - o < 16384u ? hbytes - o : 16384u, smem_u32(&S.hbar));
+    }
+    // every consumer waits (bounded), so the copy has landed before the CTA can exit
+    const bool h_ok = mbar_wait(smem_u32(&S.hbar), 0u);
+    if (!h_ok && !dead) {
+      dead = true;
+      if (lane == 0) {
+        atomicExch(err, DEVERR_RING);
+        *stop = 1;
+      }
+    }
+    float hr[HM][EL];
+    int qj[HM];
+#pragma unroll
+    for (int m = 0; m < HM; ++m) {
+      const int q = pt * Qp + lane + 32 * m;
+      qj[m] = -1;
+#pragma unroll
+      for (int e = 0; e < EL; ++e) hr[m][e] = 0.f;
+      if (q < q_end) {
+        const int j = q / C2;
+        qj[m] = (j << 16) | (q - j * C2);
+        const float4* src = reinterpret_cast<const float4*>(hs + (size_t)q * EL);
+#pragma unroll
+        for (int e = 0; e < EL / 4; ++e) {
+          const float4 v = src[e];
+          hr[m][4 * e] = v.x;
+          hr[m][4 * e + 1] = v.y;
+          hr[m][4 * e + 2] = v.z;
+          hr[m][4 * e + 3] = v.w;
+        }
+      }
+    }
+    for (; i < w.n_items; ++i) {
+      const int s = i % NS;
+      if (!dead && *stop) dead = true;
+      if (!dead) {
+        const bool ok = mbar_wait(smem_u32(&S.full[s]), (unsigned)(i / NS) & 1u);
+        if (!__all_sync(kFull, ok)) {
+          dead = true;
+          if (lane == 0) {
+            atomicExch(err, DEVERR_RING);
+            *stop = 1;
+          }
+        }
+      }
+      float* part = S.part[i & 1];
+      const RingDesc d = S.desc[s];
+      if (!dead) down_rows<F>(a, S, d, ring + (size_t)s * rc.stage_bytes, hr, qj, part, cw, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
+      consumer_sync();   // every part of every row of the item is in part[]
+      if (!dead && pt == 0 && lane == 0) {
+        for (int r = cw / kParts; r < d.n; r += kRowsPerPass) {
+          const float* pr = part + kParts * r;
+          const int n = d.p0 + r;
+          float v = (pr[0] + pr[1]) + (pr[2] + pr[3]);
+          if (a.residual) v += n - w.n0 < kMaxRows ? S.xres[n - w.n0] : x_at<F>(a, n);
+          store_out<F>(a, n, v);
+        }
+      }
+    }
+  }
+}
+
+template <int F>
+__global__ void __launch_bounds__(kRingThreads, 1) k_mlp_ring(MlpArgs a, RingCfg rc, GridBar* bar, int* err) {
+  extern __shared__ __align__(1024) uint8_t ring[];
+  __shared__ RingShared S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < a.k) {
+    S.base[threadIdx.x] = a.asg_ptr[threadIdx.x];
+    S.wt[threadIdx.x] = a.w[threadIdx.x];
+  }
+  if (a.residual) {
+    const Share w = cta_share(a, rc);
+    for (int r = threadIdx.x; r < w.n1 - w.n0 && r < kMaxRows; r += blockDim.x) S.xres[r] = x_at<F>(a, w.n0 + r);
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < rc.nstages; ++s) {
+      mbar_init(smem_u32(&S.full[s]), 1u);
+      mbar_init(smem_u32(&S.empty[s]), (unsigned)kConsumers);
+    }
+    S.stop = 0;
+    for (int q = 0; q < kMaxStages * (kConsumers / 2); ++q) (&S.cnt[0][0])[q] = 0;
+    mbar_init(smem_u32(&S.hbar), 1u);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == 0) produce<F>(a, rc, S, ring, lane, err);
+  else consume<F>(a, rc, S, ring, bar, err, warp - 1, lane);
+}
+
+// ------------------------------------------------------------------ host
+size_t host_row_bytes(int F, int K) {
+  return F == MOE_F32 ? (size_t)K * 4 : (F == MOE_BF16 ? (size_t)K * 2 : (size_t)K / 2);
+}
+
+// Stage geometry for a shape, or false if the staged kernel cannot take it.
+bool ring_geometry(int F, int H, int I, int k, RingCfg* rc, size_t* dyn_smem) {
+  if (k < 1 || k > MOE_MAX_TOPK || H < 1) return false;
+  const size_t rb1 = host_row_bytes(F, H), rb2 = host_row_bytes(F, I);
+  const int el = F == MOE_F32 ? 4 : (F == MOE_BF16 ? 8 : 32);
+  if (H % el || I % el || rb1 % 16 || rb2 % 16) return false;
+  const bool q = F == MOE_INT4_G128;
+  if (q && (H % 128 || I % 128)) return false;
+  // the consumers hold x (H / el chunks) and one part of h (ceil(k * I / el /
+  // kParts) chunks) in registers: at most 32 * XM and 32 * HM chunks per warp
+  const int xm = q ? RingTile<MOE_INT4_G128>::XM : RingTile<MOE_BF16>::XM;
+  const int hm = q ? RingTile<MOE_INT4_G128>::HM : RingTile<MOE_BF16>::HM;
+  if (H / el > 32 * xm || (k * I / el + kParts - 1) / kParts > 32 * hm) return false;
+  const size_t srb1 = q ? (size_t)(H / 128) * 2 : 0, srb2 = q ? (size_t)(I / 128) * 2 : 0;
+  // up items of kConsumers pairs (one pair per warp) while they stay small;
+  // otherwise half as many (one row per warp), so that more, smaller stages
+  // fit and a CTA's whole share of W2 can be in flight before the grid barrier
+  int P = kConsumers;
+  if ((size_t)2 * P * (rb1 + srb1) > 64 * 1024) P = kConsumers / 2;
+  if (I % P) return false;
+  size_t sb = (size_t)2 * P * (rb1 + srb1);
+  int down_rows, down_group;
+  if (q) {
+    // 8 rows of bf16 scales per expert and item keep every scale copy 16-byte aligned
+    down_group = 8;
+    down_rows = 8;
+    if (H % 8) return false;
+    sb = sb > (size_t)8 * k * (rb2 + srb2) ? sb : (size_t)8 * k * (rb2 + srb2);
+  } else {
+    down_group = 1;
+    if (sb < (size_t)k * rb2) sb = (size_t)k * rb2;
+    down_rows = (int)(sb / ((size_t)k * rb2));
+    if (down_rows > kConsumers) down_rows = kConsumers;
+  }
+  sb = (sb + 127) / 128 * 128;
+  // static shared memory (the ring starts 1024-byte aligned after it) + reserve
+  const size_t fixed = (sizeof(RingShared) + 1023) / 1024 * 1024 + 1024;
+  const size_t hbytes = ((size_t)k * I * 4 + 127) / 128 * 128;   // f32 h after the barrier
+  if (fixed + hbytes + 2 * sb > kSmemLimit) return false;
+  size_t ns = (kSmemLimit - fixed - hbytes) / sb;
+  if (ns > (size_t)kMaxStages) ns = kMaxStages;
+  rc->up_pairs = P;
+  rc->nstages = (int)ns;
+  rc->stage_bytes = (unsigned)sb;
+  rc->down_rows = down_rows;
+  rc->down_group = down_group;
+  rc->h_off = (unsigned)(ns * sb);
+  *dyn_smem = ns * sb + hbytes;
+  return true;
+}
+
+template <int F>
+struct RingState {
+  static size_t smem;        // dynamic shared memory the attribute allows
+  static int blocks_per_sm;  // occupancy at that size
+};
+template <int F>
+size_t RingState<F>::smem = 0;
+template <int F>
+int RingState<F>::blocks_per_sm = 0;
+
+constexpr int kMaxDev = 64;
+int g_sms[kMaxDev];
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) dev = 0;
+  if (g_sms[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = v > 0 ? v : 1;
+  }
+  return g_sms[dev];
+}
+
+template <int F>
+cudaError_t ring_configure_impl(int H, int I, int k) {
+  RingCfg rc;
+  size_t smem = 0;
+  if (!ring_geometry(F, H, I, k, &rc, &smem)) return cudaSuccess;   // not used for this shape
+  if (RingState<F>::smem < smem) {
+    cudaError_t e = cudaFuncSetAttribute(k_mlp_ring<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_mlp_ring<F>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    RingState<F>::smem = smem;
+  }
+  int nb = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_mlp_ring<F>, kRingThreads, smem);
+  if (e != cudaSuccess) return e;
+  RingState<F>::blocks_per_sm = nb;
+  sm_count();
+  return cudaSuccess;
+}
+
+template <int F>
+cudaError_t ring_impl(const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s) {
+  RingCfg rc;
+  size_t smem = 0;
+  if (a.T != 1 || !ring_geometry(F, a.H, a.I, a.k, &rc, &smem)) return cudaErrorNotSupported;
+  if (RingState<F>::smem < smem || RingState<F>::blocks_per_sm < 1) return cudaErrorNotSupported;
+  MlpArgs args = a;
+  void* params[] = {&args, &rc, &bar, &err};
+  return cudaLaunchCooperativeKernel((const void*)k_mlp_ring<F>, dim3(sm_count()), dim3(kRingThreads), params,
+                                     smem, s);
+}
+
+}  // namespace
+
+cudaError_t mlp_ring_configure(int wdtype, int H, int I, int k) {
+  switch (wdtype) {
+    case MOE_F32: return ring_configure_impl<MOE_F32>(H, I, k);
+    case MOE_BF16: return ring_configure_impl<MOE_BF16>(H, I, k);
+    case MOE_INT4_G128: return ring_configure_impl<MOE_INT4_G128>(H, I, k);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_mlp_ring(int wdtype, const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  switch (wdtype) {
+    case MOE_F32: return ring_impl<MOE_F32>(a, bar, err, s);
+    case MOE_BF16: return ring_impl<MOE_BF16>(a, bar, err, s);
+    case MOE_INT4_G128: return ring_impl<MOE_INT4_G128>(a, bar, err, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,479 @@
+// Grouped expert MLP for steps with many tokens (batched decode, prefill) on
+// the sm_103a tensor cores (tcgen05, bf16 operands, f32 accumulators in
+// tensor memory).
+//
+// With T tokens and top-k routing there are n = T * k assignments; expert e
+// serves the M_e assignments that chose it.  A per-token kernel would read
+// expert e's weights M_e times; here the assignments are grouped by expert
+// (k_group) and every weight tile is read once per tile of up to 128 of the
+// expert's assignments, which makes each expert a dense contraction:
+//   up:   [M_e x H] . [H x 2I]  -> h = w * silu(gate) * up   (bf16, [n, I])
+//   down: [M_e x I] . [I x H]   -> one f32 row per assignment ([n, H])
+//   combine: y[t] = sum over j of row t * k + j (+ x[t]), j in order
+// (vLLM PR #37190 "Run MoE models exceeding VRAM via expert CPU offloading
+// with GPU cache", "How it works": fused_experts over the remapped ids; the
+// expert blocks are wherever prepare put them -- pool slot, bypass scratch, or
+// mapped host memory for the cold set, "Running 125B MoE on Two 32 GB Cards",
+// section 2).
+//
+// Each output element is one tensor-core dot product over K whose value does
+// not depend on the other rows of its tile, so results do not depend on how
+// assignments are grouped or where an expert's bytes live.  INT4 weights are
+// dequantised to bf16 ((q - 8) * scale, rounded once) while being staged, and
+// h is rounded to bf16 between the two GEMMs; both stay well inside the
+// float tolerance against the float64 reference.
+//
+// Kernel shape: persistent CTAs of 8 warps, work item = (tile of <= 128
+// assignments of one expert, N tile of 128 output columns).  For each K step
+// of 64 all threads stage A (gathered activation rows) and B (weight rows) in
+// shared memory as 8 x 16-byte core matrices, one thread issues four
+// tcgen05.mma (K = 16 each) into a 128 x 128 f32 accumulator in tensor memory
+// and commits them to the stage's mbarrier; three stages let the staging of
+// the next K steps overlap the running MMAs.  The epilogue reads the
+// accumulator with tcgen05.ld.
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "internal.cuh"
+#include "mlp_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace mlp;
+
+constexpr int kGThreads = 256;                  // 8 warps
+constexpr int kTileM = 128;                     // assignments per tile (MMA M)
+constexpr int kTileN = 128;                     // output columns per item (MMA N)
+constexpr int kGStages = 3;
+constexpr int kTileBytes = kTileM * (int)tc::kTileK * 2;   // one 128 x 64 bf16 operand tile
+constexpr int kGStageBytes = 2 * kTileBytes;               // A + B
+constexpr int kGroupThreads = 1024;
+constexpr unsigned long long kGWaitNs = 500000000ull;     // 0.5 s
+
+enum { PH_UP = 0, PH_DOWN = 1 };
+
+struct GemmArgs {
+  const int32_t* order;        // [n] assignment indices grouped by expert
+  const int4* tiles;           // [ntiles] {first position in order, rows, expert, 0}
+  const int* ntiles;
+  const void* x;               // [T, H] bf16 activations (up)
+  uint16_t* hb;                // [n, I] bf16 h (written by up, read by down)
+  float* out;                  // [n, H] f32 rows, one per assignment (down)
+  const unsigned long long* asg_ptr;
+  const float* w;
+  int k, H, I;
+  unsigned long long off_w2, off_s13, off_s2;
+  int* err;
+};
+
+// ------------------------------------------------------------- grouping
+// One CTA.  Counts the assignments of every expert, lays them out expert by
+// expert (ascending expert; within an expert in no particular order, which
+// the results do not depend on) and cuts every expert's run into tiles of at
+// most kTileM.
+__global__ void __launch_bounds__(kGroupThreads, 1) k_group(const int32_t* __restrict__ ids, int n, int E,
+                                                            int32_t* __restrict__ order, int4* __restrict__ tiles,
+                                                            int* __restrict__ ntiles) {
+  __shared__ int cnt[MOE_MAX_EXPERTS];
+  __shared__ int off[MOE_MAX_EXPERTS];
+  __shared__ int toff[MOE_MAX_EXPERTS];
+  __shared__ int cur[MOE_MAX_EXPERTS];
+  __shared__ int wsum[2][kGroupThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += blockDim.x) {
+    cnt[e] = 0;
+    cur[e] = 0;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  // exclusive scans of the counts and of the tile counts (E <= blockDim.x)
+  const int c = tid < E ? cnt[tid] : 0;
+  const int t = (c + kTileM - 1) / kTileM;
+  int ic = c, it = t;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, ic, o), b = __shfl_up_sync(0xffffffffu, it, o);
+    if (lane >= o) {
+      ic += a;
+      it += b;
+    }
+  }
+  if (lane == 31) {
+    wsum[0][warp] = ic;
+    wsum[1][warp] = it;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int a = lane < kGroupThreads / 32 ? wsum[0][lane] : 0, b = lane < kGroupThreads / 32 ? wsum[1][lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int pa = __shfl_up_sync(0xffffffffu, a, o), pb = __shfl_up_sync(0xffffffffu, b, o);
+      if (lane >= o) {
+        a += pa;
+        b += pb;
+      }
+    }
+    if (lane < kGroupThreads / 32) {
+      wsum[0][lane] = a;
+      wsum[1][lane] = b;
+    }
+  }
+  __syncthreads();
+  const int base_c = warp ? wsum[0][warp - 1] : 0, base_t = warp ? wsum[1][warp - 1] : 0;
+  if (tid < E) {
+    off[tid] = base_c + ic - c;
+    toff[tid] = base_t + it - t;
+  }
+  if (tid == blockDim.x - 1) *ntiles = base_t + it;
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) order[off[e] + atomicAdd(&cur[e], 1)] = i;
+  }
+  if (tid < E) {
+    for (int q = 0; q < t; ++q) {
+      const int rows = c - q * kTileM < kTileM ? c - q * kTileM : kTileM;
+      tiles[toff[tid] + q] = make_int4(off[tid] + q * kTileM, rows, tid, 0);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- staging
+// A tile: rows r < rows of the item take activation row src_row(r) at
+// columns k0 .. k0 + 63 (bf16), the other rows are zero.  Two threads per
+// row, four 16-byte chunks each.
+__device__ __forceinline__ void stage_a(uint8_t* sm, const uint16_t* __restrict__ base, size_t row_elems,
+                                        const int32_t* __restrict__ rows_idx, int rows, int k0) {
+  const int r = threadIdx.x & (kTileM - 1);
+  const int h = threadIdx.x >> 7;   // 0 or 1
+  uint4 v[4];
+  const bool ok = r < rows;
+  const uint16_t* src = ok ? base + (size_t)rows_idx[r] * row_elems + k0 : nullptr;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = ok ? reinterpret_cast<const uint4*>(src)[h * 4 + i] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<uint4*>(sm + tc::tile_offset((uint32_t)r, (uint32_t)((h * 4 + i) * 8))) = v[i];
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// B tile, weight rows wrow(r) of an expert block at columns k0 .. k0 + 63.
+// bf16: copied; INT4: 32 codes per thread -> (q - 8) * scale, rounded to bf16.
+template <int F>
+__device__ __forceinline__ void stage_b(uint8_t* sm, const uint8_t* __restrict__ wbase, size_t row_bytes_,
+                                        const uint16_t* __restrict__ sbase, int groups, int wrow, int k0) {
+  const int r = threadIdx.x & (kTileM - 1);
+  const int h = threadIdx.x >> 7;
+  if (F == MOE_BF16) {
+    const uint4* src = reinterpret_cast<const uint4*>(wbase + (size_t)wrow * row_bytes_ + (size_t)k0 * 2);
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = src[h * 4 + i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<uint4*>(sm + tc::tile_offset((uint32_t)r, (uint32_t)((h * 4 + i) * 8))) = v[i];
+  } else {
+    // 32 codes = 16 bytes at element k0 + 32 h; one scale covers the whole tile row
+    const uint4 q = *reinterpret_cast<const uint4*>(wbase + (size_t)wrow * row_bytes_ + (size_t)(k0 + 32 * h) / 2);
+    const float s = bf16_bits(sbase[(size_t)wrow * groups + (k0 >> 7)]);
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t wd = words[i];   // elements 8 i .. 8 i + 7 of this thread's 32
+      uint4 o;
+      o.x = pack_bf16x2(code_m8(wd, 0) * s, code_m8(wd, 4) * s);
+      o.y = pack_bf16x2(code_m8(wd, 8) * s, code_m8(wd, 12) * s);
+      o.z = pack_bf16x2(code_m8(wd, 16) * s, code_m8(wd, 20) * s);
+      o.w = pack_bf16x2(code_m8(wd, 24) * s, code_m8(wd, 28) * s);
+      *reinterpret_cast<uint4*>(sm + tc::tile_offset((uint32_t)r, (uint32_t)((h * 4 + i) * 8))) = o;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ GEMM
+// PH_UP: item = (tile, N tile nt of I / 64): B rows 0..63 are gate rows
+// nt*64 .., rows 64..127 the matching up rows; K = H.  Epilogue: h.
+// PH_DOWN: item = (tile, N tile nt of H / 128): B rows are W2 rows nt*128 ..;
+// K = I.  Epilogue: f32 output rows.
+template <int F, int PH>
+__global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) unsigned long long mbar[kGStages];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int rows_idx[kTileM];     // A row source: token (up) or assignment (down)
+  __shared__ int asg_of[kTileM];       // assignment of each tile row
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntiles = *g.ntiles;
+  const int NT = PH == PH_UP ? g.I / 64 : g.H / kTileN;
+  const int items = ntiles * NT;
+  if ((int)blockIdx.x >= items) return;
+  const int K = PH == PH_UP ? g.H : g.I;
+  const int nk = K / (int)tc::kTileK;
+  const size_t rb1 = F == MOE_BF16 ? (size_t)g.H * 2 : (size_t)g.H / 2;
+  const size_t rb2 = F == MOE_BF16 ? (size_t)g.I * 2 : (size_t)g.I / 2;
+  // 1024-byte aligned stages
+  uint8_t* st0 = smem + ((1024u - (tc::smem_u32(smem) & 1023u)) & 1023u);
+  if (tid == 0) {
+    for (int s = 0; s < kGStages; ++s) tc::mbar_init(tc::smem_u32(&mbar[s]), 1u);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tc::tmem_alloc(tc::smem_u32(&tmem_slot), kTileN);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  constexpr uint32_t idesc = tc::idesc_bf16(kTileM, kTileN);
+  unsigned gs = 0;        // K steps issued by this CTA so far
+  bool dead = false;
+  for (int item = blockIdx.x; item < items && !dead; item += gridDim.x) {
+    const int tile = item / NT, nt = item - tile * NT;
+    const int4 td = g.tiles[tile];
+    const int pos0 = td.x, rows = td.y;
+    if (tid < kTileM) {
+      const int a = tid < rows ? g.order[pos0 + tid] : 0;
+      asg_of[tid] = a;
+      rows_idx[tid] = PH == PH_UP ? a / g.k : a;
+    }
+    __syncthreads();
+    const unsigned long long blk = g.asg_ptr[asg_of[0]];
+    const uint8_t* wb = reinterpret_cast<const uint8_t*>(blk) + (PH == PH_UP ? 0 : g.off_w2);
+    const uint16_t* sb = reinterpret_cast<const uint16_t*>(blk + (PH == PH_UP ? g.off_s13 : g.off_s2));
+    const int groups = (PH == PH_UP ? g.H : g.I) / 128;
+    const int r = tid & (kTileM - 1);
+    const int wrow = PH == PH_UP ? (r < 64 ? nt * 64 + r : g.I + nt * 64 + (r - 64)) : nt * kTileN + r;
+    for (int ks = 0; ks < nk; ++ks, ++gs) {
+      const int s = (int)(gs % kGStages);
+      uint8_t* sa = st0 + (size_t)s * kGStageBytes;
+      uint8_t* sbt = sa + kTileBytes;
+      if (gs >= (unsigned)kGStages) {
+        const bool ok = tc::mbar_wait(tc::smem_u32(&mbar[s]), ((gs / kGStages) - 1u) & 1u, kGWaitNs);
+        if (!ok) dead = true;
+      }
+      if (__syncthreads_or(dead)) {
+        dead = true;
+        break;
+      }
+      const int k0 = ks * (int)tc::kTileK;
+      if (PH == PH_UP) stage_a(sa, reinterpret_cast<const uint16_t*>(g.x), (size_t)g.H, rows_idx, rows, k0);
+      else stage_a(sa, g.hb, (size_t)g.I, rows_idx, rows, k0);
+      stage_b<F>(sbt, wb, PH == PH_UP ? rb1 : rb2, sb, groups, wrow, k0);
+      tc::fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tc::fence_after_sync();
+        const uint32_t a0 = tc::smem_u32(sa), b0 = tc::smem_u32(sbt);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tc::mma_bf16(tmem, tc::smem_desc(a0 + 256u * j), tc::smem_desc(b0 + 256u * j), idesc,
+                       (ks | j) != 0 ? 1u : 0u);
+        tc::mma_commit(tc::smem_u32(&mbar[s]));
+      }
+    }
+    if (dead) break;
+    // accumulator complete: the last commit covers every MMA issued before it
+    {
+      const unsigned last = gs - 1u;
+      if (!tc::mbar_wait(tc::smem_u32(&mbar[last % kGStages]), (last / kGStages) & 1u, kGWaitNs)) dead = true;
+    }
+    if (__syncthreads_or(dead)) break;
+    tc::fence_after_sync();
+    const int m = (warp & 3) * 32 + lane;            // accumulator row of this thread
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const int ch = warp >> 2;                        // column half
+    if (PH == PH_UP) {
+      uint32_t gv[32], uv[32];
+      tc::tmem_ld32(lane_base + (uint32_t)(ch * 32), gv);
+      tc::tmem_ld32(lane_base + (uint32_t)(64 + ch * 32), uv);
+      if (m < rows) {
+        const int a = asg_of[m];
+        const float wa = g.w[a];
+        uint4* dst = reinterpret_cast<uint4*>(g.hb + (size_t)a * g.I + nt * 64 + ch * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float hv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float gg = __uint_as_float(gv[8 * q + e]), uu = __uint_as_float(uv[8 * q + e]);
+            hv[e] = wa * (gg / (1.0f + expf(-gg)) * uu);
+          }
+          uint4 o;
+          o.x = pack_bf16x2(hv[0], hv[1]);
+          o.y = pack_bf16x2(hv[2], hv[3]);
+          o.z = pack_bf16x2(hv[4], hv[5]);
+          o.w = pack_bf16x2(hv[6], hv[7]);
+          dst[q] = o;
+        }
+      }
+    } else {
+      uint32_t v0[32], v1[32];
+      tc::tmem_ld32(lane_base + (uint32_t)(ch * 64), v0);
+      tc::tmem_ld32(lane_base + (uint32_t)(ch * 64 + 32), v1);
+      if (m < rows) {
+        float4* dst = reinterpret_cast<float4*>(g.out + (size_t)asg_of[m] * g.H + nt * kTileN + ch * 64);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(v0[4 * q]), __uint_as_float(v0[4 * q + 1]),
+                               __uint_as_float(v0[4 * q + 2]), __uint_as_float(v0[4 * q + 3]));
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[8 + q] = make_float4(__uint_as_float(v1[4 * q]), __uint_as_float(v1[4 * q + 1]),
+                                   __uint_as_float(v1[4 * q + 2]), __uint_as_float(v1[4 * q + 3]));
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();    // accumulator and tile tables free for the next item
+  }
+  if (dead && tid == 0) atomicExch(g.err, DEVERR_RING);
+  // every MMA this CTA issued has completed before tensor memory is freed
+  if (gs > 0 && tid == 0) {
+    const unsigned last = gs - 1u;
+    tc::mbar_wait(tc::smem_u32(&mbar[last % kGStages]), (last / kGStages) & 1u, kGWaitNs);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_free(tmem, kTileN);
+}
+
+// y[t] = sum over j of out[t * k + j] (+ x[t]), j in order
+template <int F>
+__global__ void __launch_bounds__(256) k_combine(const float* __restrict__ out, const void* __restrict__ x,
+                                                 void* __restrict__ y, int T, int k, int H, int residual) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // group of 4 columns
+  const int H4 = H / 4;
+  if (i >= (long long)T * H4) return;
+  const int t = (int)(i / H4), c4 = (int)(i - (long long)t * H4);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const float4 v = reinterpret_cast<const float4*>(out + ((size_t)t * k + j) * H)[c4];
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  const size_t o = (size_t)t * H + 4 * c4;
+  if (residual) {
+    const uint16_t* xb = reinterpret_cast<const uint16_t*>(x) + o;
+    acc.x += bf16_bits(xb[0]);
+    acc.y += bf16_bits(xb[1]);
+    acc.z += bf16_bits(xb[2]);
+    acc.w += bf16_bits(xb[3]);
+  }
+  uint2 pk;
+  pk.x = pack_bf16x2(acc.x, acc.y);
+  pk.y = pack_bf16x2(acc.z, acc.w);
+  *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(y) + o) = pk;
+}
+
+// ------------------------------------------------------------------ host
+constexpr size_t kGemmSmem = (size_t)kGStages * kGStageBytes + 1024;   // + alignment slack
+
+template <int F>
+struct GemmState {
+  static bool configured;
+  static int blocks_per_sm;
+};
+template <int F>
+bool GemmState<F>::configured = false;
+template <int F>
+int GemmState<F>::blocks_per_sm = 0;
+
+int dev_sms() {
+  int dev = 0, v = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+  return v > 0 ? v : 1;
+}
+
+template <int F>
+cudaError_t gemm_configure_impl() {
+  if (GemmState<F>::configured) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<F, PH_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_moe_gemm<F, PH_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+  if (e != cudaSuccess) return e;
+  int nb = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_moe_gemm<F, PH_UP>, kGThreads, kGemmSmem);
+  if (e != cudaSuccess) return e;
+  GemmState<F>::blocks_per_sm = nb;
+  GemmState<F>::configured = true;
+  return cudaSuccess;
+}
+
+template <int F>
+cudaError_t gemm_impl(const MlpArgs& a, const GemmBuffers& b, cudaStream_t s) {
+  if (!GemmState<F>::configured || GemmState<F>::blocks_per_sm < 1) return cudaErrorNotSupported;
+  const int n = a.T * a.k;
+  k_group<<<1, kGroupThreads, 0, s>>>(b.ids, n, b.E, b.order, b.tiles, b.ntiles);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  GemmArgs g{};
+  g.order = b.order;
+  g.tiles = b.tiles;
+  g.ntiles = b.ntiles;
+  g.x = a.x;
+  g.hb = b.hb;
+  g.out = b.out;
+  g.asg_ptr = a.asg_ptr;
+  g.w = a.w;
+  g.k = a.k;
+  g.H = a.H;
+  g.I = a.I;
+  g.off_w2 = a.off_w2;
+  g.off_s13 = a.off_s13;
+  g.off_s2 = a.off_s2;
+  g.err = b.err;
+  const int grid = GemmState<F>::blocks_per_sm * dev_sms();
+  k_moe_gemm<F, PH_UP><<<grid, kGThreads, kGemmSmem, s>>>(g);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_moe_gemm<F, PH_DOWN><<<grid, kGThreads, kGemmSmem, s>>>(g);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long groups = (long long)a.T * (a.H / 4);
+  k_combine<F><<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(b.out, a.x, a.y, a.T, a.k, a.H, a.residual);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool moe_gemm_supported(int wdtype, int H, int I, int k) {
+  if (wdtype != MOE_BF16 && wdtype != MOE_INT4_G128) return false;
+  if (k < 1 || k > MOE_MAX_TOPK) return false;
+  if (H % kTileN || I % 64) return false;          // N tiles of the two GEMMs, K tiles of 64
+  if (wdtype == MOE_INT4_G128 && (H % 128 || I % 128)) return false;
+  return true;
+}
+
+cudaError_t moe_gemm_configure(int wdtype) {
+  switch (wdtype) {
+    case MOE_BF16: return gemm_configure_impl<MOE_BF16>();
+    case MOE_INT4_G128: return gemm_configure_impl<MOE_INT4_G128>();
+  }
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_moe_gemm(int wdtype, const MlpArgs& a, const GemmBuffers& b, cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  if (!moe_gemm_supported(wdtype, a.H, a.I, a.k) || a.x == nullptr) return cudaErrorNotSupported;
+  if ((reinterpret_cast<uintptr_t>(a.x) | reinterpret_cast<uintptr_t>(a.y)) & 15) return cudaErrorNotSupported;
+  switch (wdtype) {
+    case MOE_BF16: return gemm_impl<MOE_BF16>(a, b, s);
+    case MOE_INT4_G128: return gemm_impl<MOE_INT4_G128>(a, b, s);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace moe

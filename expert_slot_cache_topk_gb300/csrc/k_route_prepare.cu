@@ -121,6 +121,21 @@ cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Every kernel of a layer step prefers the largest shared-memory carve-out,
+// so that consecutive launches (one-CTA prepare, then an expert-MLP kernel
+// with up to 227 KiB of shared memory per CTA) never make an SM switch its
+// L1 / shared-memory split in between.
+cudaError_t prepare_configure() {
+  const void* kernels[] = {(const void*)k_router, (const void*)k_prepare<256>, (const void*)k_prepare<kPrepThreads>,
+                           (const void*)k_copy};
+  for (const void* k : kernels) {
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_copy(const CopyArgs& a, int grid, cudaStream_t s) {
   k_copy<<<grid, kCopyThreads, 0, s>>>(a);
   return cudaGetLastError();

@@ -63,6 +63,12 @@ struct moe_cache {
   int scratch_n = 0;
   uint8_t* backing_h = nullptr;   // pinned, device-mapped
   uint8_t* backing_dv = nullptr;  // its device-usable address
+  bool staged_mlp = false;        // one-token steps may use the staged-weight kernel
+  bool gemm_mlp = false;          // multi-token steps may use the tensor-core grouped GEMM
+  int32_t* order_d = nullptr;     // grouped GEMM: assignments grouped by expert
+  int4* tiles_d = nullptr;        //               tiles of up to 128 assignments
+  int* ntiles_d = nullptr;
+  float* gout_d = nullptr;        //               [T*k, H] f32 per-assignment outputs
   std::vector<uint8_t> cold_h;
   bool any_cold = false;
   uint8_t* pool_d = nullptr;
@@ -186,6 +192,9 @@ moe_status device_error(moe_cache* c) {
     return fail(c, MOE_ESTATE, "device error: an expert id outside [0, E) reached prepare; that step was skipped");
   if (e == DEVERR_BARRIER)
     return fail(c, MOE_ESTATE, "device error: the fused MLP kernel's grid barrier timed out; outputs are invalid, call moe_cache_reset");
+  if (e == DEVERR_RING)
+    return fail(c, MOE_ESTATE, "device error: a staged-weight wait in the decode MLP kernel timed out; outputs are invalid, call moe_cache_reset");
+  if (e != DEVERR_NONE) return fail(c, MOE_ESTATE, "device error flag set");
   return MOE_OK;
 }
 
@@ -235,6 +244,36 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
   return MOE_OK;
 }
 
+// The expert MLP of one layer step: the staged-weight kernel for one-token
+// steps and the tensor-core grouped GEMM for multi-token steps, where the
+// shape allows it; else the cooperative up/down kernel.  `*launches` = the
+// kernels launched.  cudaErrorNotSupported (or a too-large cooperative grid)
+// = none fits; the caller then runs the separate up and down kernels.
+cudaError_t launch_layer_mlp(moe_cache* c, const MlpArgs& m, cudaStream_t s, int* launches) {
+  *launches = 1;
+  if (c->staged_mlp && m.T == 1) {
+    const cudaError_t e = launch_mlp_ring(c->wd, m, c->bar_d, c->err_d, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
+  if (c->gemm_mlp && m.T > 1) {
+    GemmBuffers b{};
+    b.ids = c->ids_d;
+    b.E = c->E;
+    b.order = c->order_d;
+    b.tiles = c->tiles_d;
+    b.ntiles = c->ntiles_d;
+    b.hb = reinterpret_cast<uint16_t*>(c->h_d);
+    b.out = c->gout_d;
+    b.err = c->err_d;
+    const cudaError_t e = launch_moe_gemm(c->wd, m, b, s);
+    if (e != cudaErrorNotSupported) {
+      *launches = 4;
+      return e;
+    }
+  }
+  return launch_mlp_fused(c->wd, m, c->bar_d, c->err_d, s);
+}
+
 // After the prepare kernel of a layer step: the missed (or, on bypass, all
 // non-cold) experts are copied on the copy stream, forked from the caller's
 // stream right after prepare and joined back before the expert MLP runs.  (An
@@ -254,9 +293,10 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
     m.tail_off = c->off_w2;
     m.tail_bytes = c->Be - c->off_w2;
     const int ti = tm_begin(c, TM_UP, s);
-    const cudaError_t fe = launch_mlp_fused(c->wd, m, c->bar_d, c->err_d, s);
+    int nl = 1;
+    const cudaError_t fe = launch_layer_mlp(c, m, s, &nl);
     if (fe == cudaSuccess) {
-      c->launches++;
+      c->launches += nl;
       tm_end(c, TM_UP, ti, s);
       tm_note_misses(c, ti, layer, s);
       return MOE_OK;
@@ -321,9 +361,10 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
   if (mlp) {
     // one cooperative launch (up, grid barrier, down); up + down if it cannot fit
     int ti = tm_begin(c, TM_UP, s);
-    const cudaError_t fe = launch_mlp_fused(c->wd, *mlp, c->bar_d, c->err_d, s);
+    int nl = 1;
+    const cudaError_t fe = launch_layer_mlp(c, *mlp, s, &nl);
     if (fe == cudaSuccess) {
-      c->launches++;
+      c->launches += nl;
       tm_end(c, TM_UP, ti, s);
       tm_note_misses(c, ti, layer, s);
       return MOE_OK;
@@ -416,7 +457,7 @@ void free_all(moe_cache* c) {
   void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->slot_map_d, c->slot_expert_d,
                  c->slot_stamp_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
                  c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->tm_miss_d, c->xs_d[0], c->xs_d[1],
-                 c->logits_stage_d};
+                 c->logits_stage_d, c->order_d, c->tiles_d, c->ntiles_d, c->gout_d};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->backing_h) cudaFreeHost(c->backing_h);
@@ -486,6 +527,8 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
     return fail(nullptr, MOE_EINVAL, "bad wdtype or shape (int4 needs hidden, inter multiples of 128)");
   if (g.hidden % chunk_elems(g.wdtype) || g.inter % chunk_elems(g.wdtype))
     return fail(nullptr, MOE_EINVAL, "hidden and inter must be multiples of 4 (f32) or 8 (bf16)");
+  if (g.mlp_kernel != MOE_MLP_AUTO && g.mlp_kernel != MOE_MLP_PLAIN)
+    return fail(nullptr, MOE_EINVAL, "mlp_kernel must be MOE_MLP_AUTO or MOE_MLP_PLAIN");
   if (g.copy_mode < MOE_COPY_AUTO || g.copy_mode > MOE_COPY_FUSED)
     return fail(nullptr, MOE_EINVAL, "bad copy_mode");
   if (g.renormalize != 0 && g.renormalize != 1) return fail(nullptr, MOE_EINVAL, "renormalize must be 0 or 1");
@@ -589,7 +632,18 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   CKC(cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming));
   CKC(cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming));
   CKC(cudaEventCreateWithFlags(&c->ev_sync, cudaEventDisableTiming));
+  CKC(prepare_configure());
   CKC(mlp_configure(c->wd, c->H, c->I, c->K));
+  c->staged_mlp = g.mlp_kernel != MOE_MLP_PLAIN;
+  if (c->staged_mlp) CKC(mlp_ring_configure(c->wd, c->H, c->I, c->K));
+  if (c->staged_mlp && c->maxT > 1 && moe_gemm_supported(c->wd, c->H, c->I, c->K)) {
+    CKC(dmalloc((void**)&c->order_d, TK * sizeof(int32_t)));
+    CKC(dmalloc((void**)&c->tiles_d, TK * sizeof(int4)));
+    CKC(dmalloc((void**)&c->ntiles_d, sizeof(int)));
+    CKC(dmalloc((void**)&c->gout_d, TK * c->H * sizeof(float)));
+    CKC(moe_gemm_configure(c->wd));
+    c->gemm_mlp = true;
+  }
   int sms = 0;
   CKC(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, g.device));
   c->copy_grid = std::max(1, sms) * 4;
@@ -721,7 +775,9 @@ moe_status moe_forward(moe_cache_t* c, int layer, const void* x_d, const float* 
   cudaStream_t s = (cudaStream_t)stream;
   st = run_prepare(c, layer, logits_d, nullptr, T, nullptr, s);
   if (st != MOE_OK) return st;
-  const MlpArgs a = mlp_args(c->wd, c->H, c->I, c->K, x_d, c->asg_d, c->w_d, c->h_d, y_d, T, flags);
+  MlpArgs a = mlp_args(c->wd, c->H, c->I, c->K, x_d, c->asg_d, c->w_d, c->h_d, y_d, T, flags);
+  a.host_lo = (unsigned long long)c->backing_dv;
+  a.host_hi = a.host_lo + (unsigned long long)c->L * c->E * c->stride;
   return run_copies_and_mlp(c, layer, s, &a);
 }
 

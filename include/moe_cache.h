@@ -90,6 +90,16 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_INT4_G128 = 2 } moe_wdtype;
  *                   reports both bandwidths and the mode chosen. */
 typedef enum { MOE_COPY_AUTO = 0, MOE_COPY_MEMCPY = 1, MOE_COPY_UVA = 2, MOE_COPY_FUSED = 3 } moe_copy_mode;
 
+/* Expert-MLP kernel of moe_forward.  AUTO: one-token steps stage the weight
+ * rows that sit in HBM through shared memory with bulk copies (one persistent
+ * CTA per SM, a producer warp and eight consumer warps), when the shape allows
+ * it (inter a multiple of 8, two stages fit in shared memory); every other step
+ * uses the cooperative up/down kernel.  PLAIN: always the cooperative kernel.
+ * Each kernel's output does not depend on where an expert's bytes live (pool,
+ * scratch, host); the two kernels sum in different orders and agree to
+ * rounding. */
+typedef enum { MOE_MLP_AUTO = 0, MOE_MLP_PLAIN = 1 } moe_mlp_kernel;
+
 typedef enum {
   MOE_OK = 0,
   MOE_EINVAL = -1,    /* bad argument, nothing done */
@@ -132,6 +142,7 @@ typedef struct {
   int copy_mode;         /* moe_copy_mode */
   int device;            /* CUDA device ordinal */
   size_t hbm_budget_bytes; /* cap on pool + scratch bytes; 0 = half of free device memory */
+  int mlp_kernel;        /* moe_mlp_kernel */
 } moe_cache_config;
 
 /* Cumulative per-layer counters (moe_cache_stats with layer = -1 sums layers).
