@@ -145,17 +145,21 @@ def peaks() -> dict:
 
 
 # DRAM bytes per launch of the roofline kernel from an ncu capture
-# (profiles/k_mlp_fused_olmoe_decode_nomiss.md), valid only while the kernel
+# (profiles/k_mlp_ring_olmoe_decode_nomiss.md), valid only while the kernel
 # source is the one that was profiled.
 MEASURED_TRAFFIC = {
-    ("olmoe", "k_mlp.cu:f2cd2368a515f0c8"): 101_358_848,
+    ("olmoe", "k_mlp_ring.cu:9069ab7720311dc4"): 103_817_600,
 }
 
 
 def kernel_source_tag() -> str:
+    """Hash of the roofline kernel's source and the shared headers it includes."""
     import hashlib
-    with open(os.path.join(ROOT, "expert_slot_cache_topk_gb300", "csrc", "k_mlp.cu"), "rb") as f:
-        return "k_mlp.cu:" + hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in ("k_mlp_ring.cu", "mlp_common.cuh"):
+        with open(os.path.join(ROOT, "expert_slot_cache_topk_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return "k_mlp_ring.cu:" + h.hexdigest()[:16]
 
 
 def cpu_cores() -> int:
@@ -268,6 +272,80 @@ def _fit_per_miss(ms: np.ndarray, misses: np.ndarray):
     A = np.stack([np.ones(len(ms)), misses.astype(np.float64)], 1)
     base, per = np.linalg.lstsq(A, ms.astype(np.float64), rcond=None)[0]
     return float(base), float(per)
+
+
+def run_prefill(args, dev, world):
+    """Prefill chunk of the prefill + cold-set workload: all layers of one
+    2048-token chunk through moe_forward (the bypass path: every non-cold
+    expert of the chunk is copied to scratch, cold experts are read in place,
+    the grouped expert MLP runs on the tensor cores).  Returns the JSON
+    object, or None when skipped."""
+    import torch
+    from expert_slot_cache_topk_gb300._abi import MOE_FWD_RESIDUAL, MoECache
+    w = synth.WORKLOADS["prefill_cold"]
+    if args.layers:
+        w = w.with_(layers=args.layers)
+    T = w.prefill_tokens
+    cold = np.stack([synth.cold_mask(w, l) for l in range(w.layers)])
+    c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, T,
+                 cold_mask=cold, copy_mode="uva", device=dev.index)
+    info = c.info()
+    for l in range(w.layers):
+        synth.fill_layer_blocks(w, l, c.backing_view(l).reshape(-1), info["slot_stride"])
+    lg = torch.from_numpy(np.stack([synth.prefill_logits(w, l) for l in range(w.layers)])).to(dev)   # [L, T, E]
+    x0 = torch.from_numpy(synth.hidden_states(w, 0, 1, tokens=T)[0].view(np.int16)).to(dev).view(torch.bfloat16)
+    ys = torch.empty((w.layers, T, w.hidden), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def chunk():
+        x = x0
+        for l in range(w.layers):
+            c.forward(l, x, lg[l], T, ys[l], MOE_FWD_RESIDUAL, stream)
+            x = ys[l]
+
+    with torch.cuda.stream(stream):
+        chunk()                                   # warm-up (the pool state does not change)
+    stream.synchronize()
+    st0 = c.stats(-1)
+    c.set_timing(True, capacity=4 * w.layers + 8)
+    reps = 2
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            chunk()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = ev0.elapsed_time(ev1) / 1e3
+    tm = c.read_timing()
+    c.set_timing(False)
+    st1 = c.stats(-1)
+    c.close()
+    max_sec, all_tok = aggregate(sec, reps * T, world, dev)
+    lay = synth.expert_layout(w.wdtype, w.hidden, w.inter)
+    # dense work of the expert MLP: 2 flops per multiply-add, 3 matrices of H x I per assignment
+    flops = reps * w.layers * T * w.top_k * 2 * 3 * w.hidden * w.inter
+    gemm_s = tm["up_ms"] / 1e3
+    copy_s = tm["copy_ms"] / 1e3
+    byp = st1["bytes_h2d_bypass"] - st0["bytes_h2d_bypass"]
+    pk = peaks()
+    tflops = flops / gemm_s / 1e12 if gemm_s > 0 else None
+    return {
+        "workload": (f"prefill chunk: {w.layers} MoE layers x {w.experts} experts, top-{w.top_k}, hidden {w.hidden}, "
+                     f"expert inter {w.inter}, int4 g128, {T} tokens, {w.slots} slots/layer (bypass), "
+                     f"{w.n_cold} cold experts/layer read in place"),
+        "value": all_tok / max_sec, "unit": "tok/s", "ms_per_chunk": 1e3 * max_sec / reps, "chunks": reps,
+        "grouped_gemm": {"kernel": "k_moe_gemm (tcgen05, group + up + down + combine)",
+                         "bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": (tflops / pk["bf16_tflops"]) if tflops else None,
+                         "flops_per_chunk": flops // reps, "ms_per_chunk": 1e3 * gemm_s / reps,
+                         "note": "INT4 weights are dequantised to bf16 on the CUDA cores while being staged"},
+        "bypass_copy": {"bytes_per_chunk": byp // reps, "ms_per_chunk": 1e3 * copy_s / reps,
+                        "gbs": byp / copy_s / 1e9 if copy_s > 0 else None},
+        "cold_reads_per_chunk": (st1["cold_reads"] - st0["cold_reads"]) // reps,
+    }
 
 
 def run_ours(args, w):
@@ -412,7 +490,7 @@ def run_ours(args, w):
                        "l2": "inputs larger than L2: every step reads "
                              f"{w.layers * w.top_k * lay['total'] / 1e9:.2f} GB of expert weights",
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "k_mlp_fused (w13 + SiLU-mul + w2, launches with no miss)",
+            "roofline": {"bound": "hbm", "kernel": "k_mlp_ring (staged-weight expert MLP: w13 + SiLU-mul + w2, launches with no miss)",
                          "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
                          "traffic": MEASURED_TRAFFIC.get((w.name, kernel_source_tag())),
@@ -422,7 +500,9 @@ def run_ours(args, w):
                     "per_miss_us": per_miss_ms * 1e3 if per_miss_ms else None,
                     "mlp_base_us": base_ms * 1e3 if base_ms is not None else None,
                     "peak_gbs": h2d_peak, "frac": (miss_gbs / h2d_peak) if (miss_gbs and h2d_peak) else None,
-                    "how": "slope of MLP-launch time vs misses in that layer step (least squares)"},
+                    "how": "slope of MLP-launch time vs misses in that layer step (least squares)",
+                    "mlp_us_by_misses": {str(m): float(mlp_ms[(mlp_miss == m) & (mlp_ms > 0)].mean() * 1e3)
+                                         for m in range(4) if ((mlp_miss == m) & (mlp_ms > 0)).any()}},
             "phases_ms_per_step": {k[:-3]: tm[k] / args.steps for k in ("route_ms", "copy_ms", "up_ms", "down_ms")},
             "cache": {k: st1[k] - st0[k] for k in ("hits", "misses", "evictions", "bypass_steps")},
             "e2e": {"value": (e2e_tok / e2e_sec) if e2e_steps > 0 else None, "unit": UNIT,
@@ -436,8 +516,12 @@ def run_ours(args, w):
             line["cpu_baseline"] = {"value": cpu_v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                                     "sample": f"{cpu_n} (token, layer) steps of the first 2 decode tokens "
                                               f"in {cpu_dt:.1f} s (float64 numpy, BLAS threads as installed)"}
-        print(json.dumps(line), flush=True)
     c.close()
+    prefill = None if args.no_prefill else run_prefill(args, dev, world)
+    if rank == 0:
+        if prefill is not None:
+            line["prefill"] = prefill
+        print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -458,6 +542,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-chunk measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -248,16 +248,30 @@ __device__ __forceinline__ void rows_dot(const uint4* const (&row)[NR], const ui
   constexpr int XM = RingTile<F>::XM;
   uint4 wv[NR][XM];
   float sc[NR][XM];
+  if (ring) {
+    // branch-free: chunks past the row end re-read its last chunk; their x is
+    // zero, so they add nothing
 #pragma unroll
-  for (int m = 0; m < XM; ++m) {
-    const int c = lane + 32 * m;
+    for (int m = 0; m < XM; ++m) {
+      const int c = min(lane + 32 * m, C - 1);
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      wv[r][m] = make_uint4(0u, 0u, 0u, 0u);
-      sc[r][m] = 0.f;
-      if (c < C) {
-        wv[r][m] = ring ? row[r][c] : __ldcs(row[r] + c);
-        if (F == MOE_INT4_G128) sc[r][m] = bf16_bits(srow[r][c >> 2]);
+      for (int r = 0; r < NR; ++r) {
+        wv[r][m] = row[r][c];
+        sc[r][m] = F == MOE_INT4_G128 ? bf16_bits(srow[r][c >> 2]) : 0.f;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < XM; ++m) {
+      const int c = lane + 32 * m;
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        wv[r][m] = make_uint4(0u, 0u, 0u, 0u);
+        sc[r][m] = 0.f;
+        if (c < C) {
+          wv[r][m] = __ldcs(row[r] + c);
+          if (F == MOE_INT4_G128) sc[r][m] = bf16_bits(srow[r][c >> 2]);
+        }
       }
     }
   }
@@ -379,6 +393,48 @@ __device__ __forceinline__ void down_rows(const MlpArgs& a, const RingShared& S,
       }
     }
   }
+  if (d.src == 0u) {
+    // every expert of the item is in the ring: branch-free loads (chunks past
+    // the part's end read offset 0; their h is zero, so they add nothing)
+    for (int r0 = cw / kParts; r0 < d.n; r0 += 2 * kRowsPerPass) {
+      const int r1 = r0 + kRowsPerPass;
+      const bool two = r1 < d.n;
+      const int r1c = two ? r1 : r0;
+      uint4 w0[HM], w1[HM];
+      float s0[HM], s1[HM];
+#pragma unroll
+      for (int m = 0; m < HM; ++m) {
+        const uint32_t o = off[m] == 0xffffffffu ? 0u : off[m];
+        w0[m] = *reinterpret_cast<const uint4*>(stage + o + (size_t)r0 * rb2);
+        w1[m] = *reinterpret_cast<const uint4*>(stage + o + (size_t)r1c * rb2);
+        if (F == MOE_INT4_G128) {
+          const uint16_t* sp = reinterpret_cast<const uint16_t*>(sring + soff[m]);
+          s0[m] = bf16_bits(sp[(size_t)r0 * G2]);
+          s1[m] = bf16_bits(sp[(size_t)r1c * G2]);
+        }
+      }
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < HM; ++m) {
+        const float d0 = chunk_dot_r<F>(w0[m], hr[m]);
+        const float d1 = chunk_dot_r<F>(w1[m], hr[m]);
+        if (F == MOE_INT4_G128) {
+          acc0 = fmaf(d0, s0[m], acc0);
+          acc1 = fmaf(d1, s1[m], acc1);
+        } else {
+          acc0 += d0;
+          acc1 += d1;
+        }
+      }
+      acc0 = warp_sum(acc0);
+      acc1 = warp_sum(acc1);
+      if (lane == 0) {
+        part[kParts * r0 + cw % kParts] = acc0;
+        if (two) part[kParts * r1 + cw % kParts] = acc1;
+      }
+    }
+    return;
+  }
   for (int r0 = cw / kParts; r0 < d.n; r0 += 2 * kRowsPerPass) {
     const int r1 = r0 + kRowsPerPass;
     const bool two = r1 < d.n;
@@ -432,11 +488,11 @@ __device__ __forceinline__ void down_rows(const MlpArgs& a, const RingShared& S,
 
 // ------------------------------------------------------------- producer
 // Items of CTA b of G: up items = groups of P = up_pairs consecutive row
-// pairs of one assignment, groups [b*NG/G, (b+1)*NG/G) of NG = k * I / P
-// (expert-major); then down items = runs of down_rows output rows of the
-// CTA's row range (whole groups of down_group rows).
+// pairs of one assignment, groups b, b + G, b + 2 G, ... of the NG = k * I / P
+// groups (expert-major); then down items = runs of down_rows output rows of
+// the CTA's row range (whole groups of down_group rows).
 struct Share {
-  int g_beg, g_end;   // up groups
+  int g0, gstride;    // up groups g0, g0 + gstride, ... (below ng)
   int n0, n1;         // output rows
   int n_up, n_items;
 };
@@ -445,12 +501,14 @@ __device__ __forceinline__ Share cta_share(const MlpArgs& a, const RingCfg& rc) 
   Share w;
   const long long G = gridDim.x, b = blockIdx.x;
   const long long ng = (long long)a.k * (a.I / rc.up_pairs);
-  w.g_beg = (int)(ng * b / G);
-  w.g_end = (int)(ng * (b + 1) / G);
+  // groups round-robin over the CTAs, so that every expert -- in particular
+  // one read from host memory in this step -- is spread over many CTAs
+  w.g0 = (int)b;
+  w.gstride = (int)G;
+  w.n_up = b < ng ? (int)((ng - 1 - b) / G + 1) : 0;
   const long long nrg = a.H / rc.down_group;
   w.n0 = (int)(nrg * b / G) * rc.down_group;
   w.n1 = (int)(nrg * (b + 1) / G) * rc.down_group;
-  w.n_up = w.g_end - w.g_beg;
   w.n_items = w.n_up + (w.n1 - w.n0 + rc.down_rows - 1) / rc.down_rows;
   return w;
 }
@@ -489,7 +547,7 @@ __device__ __forceinline__ void produce(const MlpArgs& a, const RingCfg& rc, Rin
       break;
     }
     if (i < w.n_up) {
-      const int gg = w.g_beg + i;
+      const int gg = w.g0 + i * w.gstride;
       const int j = gg / gpe;
       const int p0 = (gg - j * gpe) * P;
       const unsigned long long blk = __shfl_sync(kFull, myb, j);
@@ -549,9 +607,10 @@ __device__ __forceinline__ void consume(const MlpArgs& a, const RingCfg& rc, Rin
   const int NS = rc.nstages;
   const int ctid = cw * 32 + lane;
   volatile int* stop = &S.stop;
-  // read-through: this CTA's share of the copies of the missed experts' bytes
-  // after w13 (w2 and scales) into their slots, 4 KiB per task; they complete
-  // before the grid barrier, so the down items may read them from the slots
+  // read-through: copies of the missed experts' bytes after w13 (w2 and
+  // scales) into their slots, 4 KiB per task, an equal share per CTA.  They
+  // complete before the grid barrier, so the down items may read them from
+  // the slots.
   if (a.readthrough) {
     const unsigned pend = __ballot_sync(kFull, lane < a.k && a.pending[lane] != 0 && S.base[lane] != 0ull);
     if (pend) {
@@ -559,23 +618,23 @@ __device__ __forceinline__ void consume(const MlpArgs& a, const RingCfg& rc, Rin
       const unsigned long long ncopy = (unsigned long long)__popc(pend) * cpe;
       const unsigned long long c_beg = ncopy * blockIdx.x / gridDim.x;
       const unsigned long long c_end = ncopy * (blockIdx.x + 1) / gridDim.x;
+      const unsigned long long nv_all = a.tail_bytes / 16ull;
       for (unsigned long long c = c_beg + cw; c < c_end; c += kConsumers) {
         const int sidx = (int)(c / cpe);
-        const unsigned long long off = a.tail_off + (c - (unsigned long long)sidx * cpe) * 4096ull;
-        const int asg = nth_set_bit(pend, sidx);
-        const uint4* src = reinterpret_cast<const uint4*>(a.src_ptr[asg] + off);
-        uint4* dst = reinterpret_cast<uint4*>(S.base[asg] + off);
-        const unsigned long long nv = (a.tail_off + a.tail_bytes - off) / 16ull;
+        const unsigned long long v0 = (c - (unsigned long long)sidx * cpe) * 256ull;   // 4 KiB = 256 vectors
+        const int j = nth_set_bit(pend, sidx);
+        const uint4* src = reinterpret_cast<const uint4*>(a.src_ptr[j] + a.tail_off);
+        uint4* dst = reinterpret_cast<uint4*>(S.base[j] + a.tail_off);
         uint4 v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const unsigned q = lane + 32u * u;
-          if (q < nv) v[u] = __ldcs(src + q);
+          const unsigned long long q = v0 + lane + 32u * u;
+          if (q < nv_all) v[u] = __ldcs(src + q);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const unsigned q = lane + 32u * u;
-          if (q < nv) dst[q] = v[u];
+          const unsigned long long q = v0 + lane + 32u * u;
+          if (q < nv_all) dst[q] = v[u];
         }
       }
     }

@@ -25,12 +25,12 @@
 //
 // Kernel shape: persistent CTAs of 8 warps, work item = (tile of <= 128
 // assignments of one expert, N tile of 128 output columns).  For each K step
-// of 64 all threads stage A (gathered activation rows) and B (weight rows) in
-// shared memory as 8 x 16-byte core matrices, one thread issues four
-// tcgen05.mma (K = 16 each) into a 128 x 128 f32 accumulator in tensor memory
-// and commits them to the stage's mbarrier; three stages let the staging of
-// the next K steps overlap the running MMAs.  The epilogue reads the
-// accumulator with tcgen05.ld.
+// of 64 the threads stage A (gathered activation rows) and B (weight rows) in
+// shared memory as 8 x 16-byte core matrices with cp.async, two K steps ahead
+// of the MMAs over four stages; one thread issues four tcgen05.mma (K = 16
+// each) into a 128 x 128 f32 accumulator in tensor memory and commits them to
+// the stage's mbarrier, which releases the stage for the next copies.  The
+// epilogue reads the accumulator with tcgen05.ld.
 
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -48,7 +48,6 @@ using namespace mlp;
 constexpr int kGThreads = 256;                  // 8 warps
 constexpr int kTileM = 128;                     // assignments per tile (MMA M)
 constexpr int kTileN = 128;                     // output columns per item (MMA N)
-constexpr int kGStages = 3;
 constexpr int kTileBytes = kTileM * (int)tc::kTileK * 2;   // one 128 x 64 bf16 operand tile
 constexpr int kGStageBytes = 2 * kTileBytes;               // A + B
 constexpr int kGroupThreads = 1024;
@@ -147,59 +146,22 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const int32_t* __res
 }
 
 // ---------------------------------------------------------------- staging
-// A tile: rows r < rows of the item take activation row src_row(r) at
-// columns k0 .. k0 + 63 (bf16), the other rows are zero.  Two threads per
-// row, four 16-byte chunks each.
-__device__ __forceinline__ void stage_a(uint8_t* sm, const uint16_t* __restrict__ base, size_t row_elems,
-                                        const int32_t* __restrict__ rows_idx, int rows, int k0) {
-  const int r = threadIdx.x & (kTileM - 1);
-  const int h = threadIdx.x >> 7;   // 0 or 1
-  uint4 v[4];
-  const bool ok = r < rows;
-  const uint16_t* src = ok ? base + (size_t)rows_idx[r] * row_elems + k0 : nullptr;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = ok ? reinterpret_cast<const uint4*>(src)[h * 4 + i] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    *reinterpret_cast<uint4*>(sm + tc::tile_offset((uint32_t)r, (uint32_t)((h * 4 + i) * 8))) = v[i];
+// Thread t stages row r = t % 128 of both 128 x 64 operand tiles, chunks
+// 4 h .. 4 h + 3 (h = t / 128) of 8 bf16 each.  A rows and bf16 weight rows
+// go straight into the core-matrix layout with cp.async (16 bytes, L2 only);
+// INT4 weight rows (16 bytes = 32 codes per thread) go to a raw buffer and are
+// dequantised by the same thread once they have landed.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&p);
-}
-
-// B tile, weight rows wrow(r) of an expert block at columns k0 .. k0 + 63.
-// bf16: copied; INT4: 32 codes per thread -> (q - 8) * scale, rounded to bf16.
-template <int F>
-__device__ __forceinline__ void stage_b(uint8_t* sm, const uint8_t* __restrict__ wbase, size_t row_bytes_,
-                                        const uint16_t* __restrict__ sbase, int groups, int wrow, int k0) {
-  const int r = threadIdx.x & (kTileM - 1);
-  const int h = threadIdx.x >> 7;
-  if (F == MOE_BF16) {
-    const uint4* src = reinterpret_cast<const uint4*>(wbase + (size_t)wrow * row_bytes_ + (size_t)k0 * 2);
-    uint4 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = src[h * 4 + i];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      *reinterpret_cast<uint4*>(sm + tc::tile_offset((uint32_t)r, (uint32_t)((h * 4 + i) * 8))) = v[i];
-  } else {
-    // 32 codes = 16 bytes at element k0 + 32 h; one scale covers the whole tile row
-    const uint4 q = *reinterpret_cast<const uint4*>(wbase + (size_t)wrow * row_bytes_ + (size_t)(k0 + 32 * h) / 2);
-    const float s = bf16_bits(sbase[(size_t)wrow * groups + (k0 >> 7)]);
-    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t wd = words[i];   // elements 8 i .. 8 i + 7 of this thread's 32
-      uint4 o;
-      o.x = pack_bf16x2(code_m8(wd, 0) * s, code_m8(wd, 4) * s);
-      o.y = pack_bf16x2(code_m8(wd, 8) * s, code_m8(wd, 12) * s);
-      o.z = pack_bf16x2(code_m8(wd, 16) * s, code_m8(wd, 20) * s);
-      o.w = pack_bf16x2(code_m8(wd, 24) * s, code_m8(wd, 28) * s);
-      *reinterpret_cast<uint4*>(sm + tc::tile_offset((uint32_t)r, (uint32_t)((h * 4 + i) * 8))) = o;
-    }
-  }
 }
 
 // ------------------------------------------------------------------ GEMM
@@ -207,10 +169,15 @@ __device__ __forceinline__ void stage_b(uint8_t* sm, const uint8_t* __restrict__
 // nt*64 .., rows 64..127 the matching up rows; K = H.  Epilogue: h.
 // PH_DOWN: item = (tile, N tile nt of H / 128): B rows are W2 rows nt*128 ..;
 // K = I.  Epilogue: f32 output rows.
+constexpr int kGStagesP = 4;                 // staged K steps
+constexpr int kGAhead = 2;                   // K steps in flight ahead of the MMA
+constexpr int kRawBytes = kTileM * 2 * 16;   // INT4 raw rows of one K step
+constexpr int kMaxGroups = 64;               // scale groups per row kept in shared memory (K <= 8192)
+
 template <int F, int PH>
 __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) unsigned long long mbar[kGStages];
+  __shared__ __align__(8) unsigned long long mbar[kGStagesP];
   __shared__ uint32_t tmem_slot;
   __shared__ int rows_idx[kTileM];     // A row source: token (up) or assignment (down)
   __shared__ int asg_of[kTileM];       // assignment of each tile row
@@ -221,12 +188,15 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
   if ((int)blockIdx.x >= items) return;
   const int K = PH == PH_UP ? g.H : g.I;
   const int nk = K / (int)tc::kTileK;
-  const size_t rb1 = F == MOE_BF16 ? (size_t)g.H * 2 : (size_t)g.H / 2;
-  const size_t rb2 = F == MOE_BF16 ? (size_t)g.I * 2 : (size_t)g.I / 2;
-  // 1024-byte aligned stages
-  uint8_t* st0 = smem + ((1024u - (tc::smem_u32(smem) & 1023u)) & 1023u);
+  const size_t wrb = PH == PH_UP ? (F == MOE_BF16 ? (size_t)g.H * 2 : (size_t)g.H / 2)
+                                 : (F == MOE_BF16 ? (size_t)g.I * 2 : (size_t)g.I / 2);
+  const int groups = K / 128;          // INT4 scale groups per weight row
+  // layout: [stages x (A tile | B tile)] [stages x raw INT4] [128 x groups scales]
+  uint8_t* base = smem + ((1024u - (tc::smem_u32(smem) & 1023u)) & 1023u);
+  uint8_t* raw0 = base + (size_t)kGStagesP * kGStageBytes;
+  uint16_t* sc = reinterpret_cast<uint16_t*>(raw0 + (size_t)kGStagesP * kRawBytes);
   if (tid == 0) {
-    for (int s = 0; s < kGStages; ++s) tc::mbar_init(tc::smem_u32(&mbar[s]), 1u);
+    for (int s = 0; s < kGStagesP; ++s) tc::mbar_init(tc::smem_u32(&mbar[s]), 1u);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&tmem_slot), kTileN);
@@ -235,7 +205,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
   constexpr uint32_t idesc = tc::idesc_bf16(kTileM, kTileN);
-  unsigned gs = 0;        // K steps issued by this CTA so far
+  const int r = tid & (kTileM - 1);
+  const int hh = tid >> 7;             // which 32-element half of the K step this thread stages
+  unsigned gs = 0;                     // K steps of this CTA so far (stage = gs % kGStagesP)
   bool dead = false;
   for (int item = blockIdx.x; item < items && !dead; item += gridDim.x) {
     const int tile = item / NT, nt = item - tile * NT;
@@ -249,28 +221,87 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
     __syncthreads();
     const unsigned long long blk = g.asg_ptr[asg_of[0]];
     const uint8_t* wb = reinterpret_cast<const uint8_t*>(blk) + (PH == PH_UP ? 0 : g.off_w2);
-    const uint16_t* sb = reinterpret_cast<const uint16_t*>(blk + (PH == PH_UP ? g.off_s13 : g.off_s2));
-    const int groups = (PH == PH_UP ? g.H : g.I) / 128;
-    const int r = tid & (kTileM - 1);
+    const uint16_t* sbase = reinterpret_cast<const uint16_t*>(blk + (PH == PH_UP ? g.off_s13 : g.off_s2));
     const int wrow = PH == PH_UP ? (r < 64 ? nt * 64 + r : g.I + nt * 64 + (r - 64)) : nt * kTileN + r;
-    for (int ks = 0; ks < nk; ++ks, ++gs) {
-      const int s = (int)(gs % kGStages);
-      uint8_t* sa = st0 + (size_t)s * kGStageBytes;
-      uint8_t* sbt = sa + kTileBytes;
-      if (gs >= (unsigned)kGStages) {
-        const bool ok = tc::mbar_wait(tc::smem_u32(&mbar[s]), ((gs / kGStages) - 1u) & 1u, kGWaitNs);
-        if (!ok) dead = true;
+    const uint8_t* wrow_p = wb + (size_t)wrow * wrb;
+    const bool arow_ok = r < rows;
+    const uint8_t* arow_p = PH == PH_UP
+                                ? reinterpret_cast<const uint8_t*>(g.x) + (size_t)rows_idx[arow_ok ? r : 0] * g.H * 2
+                                : reinterpret_cast<const uint8_t*>(g.hb) + (size_t)rows_idx[arow_ok ? r : 0] * g.I * 2;
+    if (F == MOE_INT4_G128) {
+      // this item's scales: 128 rows x groups, two threads per row
+      for (int q = hh; q < groups; q += 2) sc[r * kMaxGroups + q] = sbase[(size_t)wrow * groups + q];
+    }
+    // stage the operands of K step ks (global step gq) into stage gq % kGStagesP
+    auto issue = [&](int ks, unsigned gq) {
+      const int s = (int)(gq % kGStagesP);
+      uint8_t* sa = base + (size_t)s * kGStageBytes;
+      const uint32_t sa_u = tc::smem_u32(sa), sb_u = sa_u + kTileBytes;
+      const int k0 = ks * (int)tc::kTileK;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t kk = (uint32_t)((hh * 4 + i) * 8);
+        cp_async16(sa_u + tc::tile_offset((uint32_t)r, kk), arow_p + (size_t)(k0 + kk) * 2, arow_ok);
       }
+      if (F == MOE_BF16) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t kk = (uint32_t)((hh * 4 + i) * 8);
+          cp_async16(sb_u + tc::tile_offset((uint32_t)r, kk), wrow_p + (size_t)(k0 + kk) * 2, true);
+        }
+      } else {
+        cp_async16(tc::smem_u32(raw0 + (size_t)s * kRawBytes + (size_t)tid * 16),
+                   wrow_p + (size_t)(k0 + 32 * hh) / 2, true);
+      }
+    };
+    for (int q = 0; q < kGAhead; ++q) {
+      if (q < nk) {
+        const unsigned gq = gs + q;
+        if (gq >= (unsigned)kGStagesP &&
+            !tc::mbar_wait(tc::smem_u32(&mbar[gq % kGStagesP]), ((gq / kGStagesP) - 1u) & 1u, kGWaitNs))
+          dead = true;
+        issue(q, gq);
+      }
+      cp_async_commit();
+    }
+    __syncthreads();   // scales in shared memory
+    for (int ks = 0; ks < nk; ++ks, ++gs) {
+      const int s = (int)(gs % kGStagesP);
+      // prefetch K step ks + kGAhead once the MMA that last used its stage is done
+      {
+        const int kp = ks + kGAhead;
+        if (kp < nk) {
+          const unsigned gq = gs + kGAhead;
+          if (gq >= (unsigned)kGStagesP &&
+              !tc::mbar_wait(tc::smem_u32(&mbar[gq % kGStagesP]), ((gq / kGStagesP) - 1u) & 1u, kGWaitNs))
+            dead = true;
+          issue(kp, gq);
+        }
+        cp_async_commit();
+      }
+      cp_async_wait<kGAhead>();          // this thread's copies of step ks have landed
+      uint8_t* sa = base + (size_t)s * kGStageBytes;
+      uint8_t* sbt = sa + kTileBytes;
+      if (F == MOE_INT4_G128) {
+        const uint4 qv = *reinterpret_cast<const uint4*>(raw0 + (size_t)s * kRawBytes + (size_t)tid * 16);
+        const float scl = bf16_bits(sc[r * kMaxGroups + ((ks * (int)tc::kTileK) >> 7)]);
+        const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t wd = words[i];   // elements 8 i .. 8 i + 7 of this thread's 32
+          uint4 o;
+          o.x = pack_bf16x2(code_m8(wd, 0) * scl, code_m8(wd, 4) * scl);
+          o.y = pack_bf16x2(code_m8(wd, 8) * scl, code_m8(wd, 12) * scl);
+          o.z = pack_bf16x2(code_m8(wd, 16) * scl, code_m8(wd, 20) * scl);
+          o.w = pack_bf16x2(code_m8(wd, 24) * scl, code_m8(wd, 28) * scl);
+          *reinterpret_cast<uint4*>(sbt + tc::tile_offset((uint32_t)r, (uint32_t)((hh * 4 + i) * 8))) = o;
+        }
+      }
+      tc::fence_async_smem();
       if (__syncthreads_or(dead)) {
         dead = true;
         break;
       }
-      const int k0 = ks * (int)tc::kTileK;
-      if (PH == PH_UP) stage_a(sa, reinterpret_cast<const uint16_t*>(g.x), (size_t)g.H, rows_idx, rows, k0);
-      else stage_a(sa, g.hb, (size_t)g.I, rows_idx, rows, k0);
-      stage_b<F>(sbt, wb, PH == PH_UP ? rb1 : rb2, sb, groups, wrow, k0);
-      tc::fence_async_smem();
-      __syncthreads();
       if (tid == 0) {
         tc::fence_after_sync();
         const uint32_t a0 = tc::smem_u32(sa), b0 = tc::smem_u32(sbt);
@@ -281,11 +312,12 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
         tc::mma_commit(tc::smem_u32(&mbar[s]));
       }
     }
+    cp_async_wait<0>();
     if (dead) break;
     // accumulator complete: the last commit covers every MMA issued before it
     {
       const unsigned last = gs - 1u;
-      if (!tc::mbar_wait(tc::smem_u32(&mbar[last % kGStages]), (last / kGStages) & 1u, kGWaitNs)) dead = true;
+      if (!tc::mbar_wait(tc::smem_u32(&mbar[last % kGStagesP]), (last / kGStagesP) & 1u, kGWaitNs)) dead = true;
     }
     if (__syncthreads_or(dead)) break;
     tc::fence_after_sync();
@@ -333,13 +365,14 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
       }
     }
     tc::fence_before_sync();
-    __syncthreads();    // accumulator and tile tables free for the next item
+    __syncthreads();    // accumulator, tile tables and scales free for the next item
   }
+  cp_async_wait<0>();
   if (dead && tid == 0) atomicExch(g.err, DEVERR_RING);
   // every MMA this CTA issued has completed before tensor memory is freed
   if (gs > 0 && tid == 0) {
     const unsigned last = gs - 1u;
-    tc::mbar_wait(tc::smem_u32(&mbar[last % kGStages]), (last / kGStages) & 1u, kGWaitNs);
+    tc::mbar_wait(tc::smem_u32(&mbar[last % kGStagesP]), (last / kGStagesP) & 1u, kGWaitNs);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -378,7 +411,8 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ out, 
 }
 
 // ------------------------------------------------------------------ host
-constexpr size_t kGemmSmem = (size_t)kGStages * kGStageBytes + 1024;   // + alignment slack
+constexpr size_t kGemmSmem = (size_t)kGStagesP * (kGStageBytes + kRawBytes) +
+                             (size_t)kTileM * kMaxGroups * 2 + 1024;   // + alignment slack
 
 template <int F>
 struct GemmState {
@@ -400,10 +434,14 @@ int dev_sms() {
 template <int F>
 cudaError_t gemm_configure_impl() {
   if (GemmState<F>::configured) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<F, PH_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_moe_gemm<F, PH_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-  if (e != cudaSuccess) return e;
+  const void* kernels[] = {(const void*)k_moe_gemm<F, PH_UP>, (const void*)k_moe_gemm<F, PH_DOWN>};
+  for (const void* kf : kernels) {
+    cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kf, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e;
   int nb = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_moe_gemm<F, PH_UP>, kGThreads, kGemmSmem);
   if (e != cudaSuccess) return e;
@@ -453,6 +491,7 @@ bool moe_gemm_supported(int wdtype, int H, int I, int k) {
   if (wdtype != MOE_BF16 && wdtype != MOE_INT4_G128) return false;
   if (k < 1 || k > MOE_MAX_TOPK) return false;
   if (H % kTileN || I % 64) return false;          // N tiles of the two GEMMs, K tiles of 64
+  if (H > 128 * kMaxGroups || I > 128 * kMaxGroups) return false;   // scales of an item in shared memory
   if (wdtype == MOE_INT4_G128 && (H % 128 || I % 128)) return false;
   return true;
 }
