@@ -537,6 +537,7 @@ def main():
     ap.add_argument("--workload", default="olmoe", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--copy-mode", default="auto", choices=["auto", "uva", "memcpy", "fused"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling case)")
+    ap.add_argument("--slots", type=int, default=-1, help="override the pool slots per layer (N)")
     ap.add_argument("--clock-ms", type=int, default=100, help="nvidia-smi sampling interval in ms")
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
@@ -549,6 +550,8 @@ def main():
     w = synth.WORKLOADS[args.workload]
     if args.layers:
         w = w.with_(layers=args.layers)
+    if args.slots >= 0:
+        w = w.with_(slots=args.slots)
     if args.impl == "reference":
         run_reference(args, w)
     else:
