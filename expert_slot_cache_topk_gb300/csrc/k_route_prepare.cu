@@ -111,8 +111,10 @@ cudaError_t launch_router(const float* logits, int T, int E, int k, int renorm, 
 
 cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s) {
   // one thread per expert for the ranking scans, one warp per token for the
-  // fused router (at most 32 warps)
+  // fused router, plus (when it fits) E more threads so that the slot state
+  // is loaded by threads that do not route
   int need = a.E > 32 * a.T ? a.E : 32 * a.T;
+  if (a.do_route && a.E + 32 * a.T <= kPrepThreads && a.E + 32 * a.T > need) need = a.E + 32 * a.T;
   if (need > kPrepThreads) need = kPrepThreads;
   const int threads = (need + 31) / 32 * 32;
   if (a.do_route && a.T * a.k > prep::kMaxRoutedIds) return cudaErrorInvalidValue;

@@ -159,6 +159,7 @@ struct PrepSmem {
   int victim[MOE_MAX_EXPERTS];
   unsigned char mark[MOE_MAX_EXPERTS];
   unsigned char newf[MOE_MAX_EXPERTS];   // expert copied in this step
+  unsigned long long stats[ST_COUNT];    // the layer's counters, read at the start
   unsigned char cold[MOE_MAX_EXPERTS];
   int32_t ids[kMaxRoutedIds];
   int bad;
@@ -173,19 +174,24 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
   const int n_ids = a.T * a.k;
   const bool ids_in_smem = a.do_route != 0;
 
-  // every global read the step needs, issued before anything waits
+  // every global read the step needs, issued before anything waits.  With
+  // the fused router the first a.T warps route (their logits loads go out at
+  // once) and the threads after them load the slot state, so the two
+  // latencies overlap.
   const unsigned long long clk = a.st->clock;
   const int nfree = a.st->nfree;
-  if (tid < E) {
-    S.map[tid] = a.slot_map[tid];
-    S.cold[tid] = a.cold != nullptr ? a.cold[tid] : 0;
-    S.mark[tid] = 0;
-    S.newf[tid] = 0;
+  const int l0 = (a.do_route && nthr >= 32 * a.T + 32) ? 32 * a.T : 0;   // first state-loading thread
+  for (int q = tid - l0; q >= 0 && q < E; q += nthr - l0) {
+    S.map[q] = a.slot_map[q];
+    S.cold[q] = a.cold != nullptr ? a.cold[q] : 0;
+    S.mark[q] = 0;
+    S.newf[q] = 0;
   }
-  if (tid < N) {
-    S.sexp[tid] = a.slot_expert[tid];
-    S.stamp[tid] = a.slot_stamp[tid];
+  for (int q = tid - l0; q >= 0 && q < N; q += nthr - l0) {
+    S.sexp[q] = a.slot_expert[q];
+    S.stamp[q] = a.slot_stamp[q];
   }
+  if (tid - l0 >= 0 && tid - l0 < ST_COUNT) S.stats[tid - l0] = a.st->stats[tid - l0];
   if (tid == 0) S.bad = 0;
   if (a.do_route) {
     for (int t = tid >> 5; t < a.T; t += nthr / 32)
@@ -288,7 +294,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
     LayerState* st = a.st;
     unsigned long long sv[ST_COUNT];
 #pragma unroll
-    for (int i = 0; i < ST_COUNT; ++i) sv[i] = st->stats[i];
+    for (int i = 0; i < ST_COUNT; ++i) sv[i] = S.stats[i];
     if (n_ids > 0) sv[ST_STEPS] += 1;
     sv[ST_COLD] += (unsigned long long)C;
     sv[ST_B_COLD] += (unsigned long long)C * a.expert_bytes;
