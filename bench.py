@@ -285,6 +285,8 @@ def run_prefill(args, dev, world):
     w = synth.WORKLOADS["prefill_cold"]
     if args.layers:
         w = w.with_(layers=args.layers)
+    if args.prefill_slots >= 0:
+        w = w.with_(slots=args.prefill_slots)
     T = w.prefill_tokens
     cold = np.stack([synth.cold_mask(w, l) for l in range(w.layers)])
     c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, T,
@@ -304,7 +306,7 @@ def run_prefill(args, dev, world):
             x = ys[l]
 
     with torch.cuda.stream(stream):
-        chunk()                                   # warm-up (the pool state does not change)
+        chunk()                                   # warm-up (a bypass chunk leaves the pool as it is)
     stream.synchronize()
     st0 = c.stats(-1)
     c.set_timing(True, capacity=4 * w.layers + 8)
@@ -334,7 +336,8 @@ def run_prefill(args, dev, world):
     tflops = flops / gemm_s / 1e12 if gemm_s > 0 else None
     return {
         "workload": (f"prefill chunk: {w.layers} MoE layers x {w.experts} experts, top-{w.top_k}, hidden {w.hidden}, "
-                     f"expert inter {w.inter}, int4 g128, {T} tokens, {w.slots} slots/layer (bypass), "
+                     f"expert inter {w.inter}, int4 g128, {T} tokens, {w.slots} slots/layer"
+                     f"{' (bypass)' if w.slots < w.experts - w.n_cold else ' (all non-cold resident)'}, "
                      f"{w.n_cold} cold experts/layer read in place"),
         "value": all_tok / max_sec, "unit": "tok/s", "ms_per_chunk": 1e3 * max_sec / reps, "chunks": reps,
         "grouped_gemm": {"kernel": "k_moe_gemm (tcgen05, group + up + down + combine)",
@@ -544,6 +547,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-chunk measurement")
+    ap.add_argument("--prefill-slots", type=int, default=-1, help="pool slots per layer for the prefill chunk")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

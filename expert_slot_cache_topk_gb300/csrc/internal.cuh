@@ -31,6 +31,7 @@ struct LayerState {
 // [LST_COUNT][E] int32 block per layer.
 struct RecHdr {
   int n_ids, bypass, n_distinct, n_cold, n_noncold, n_hits, n_misses, n_evictions;
+  unsigned seq;   // unique number of this prepare call (per handle)
 };
 enum { LST_HITS = 0, LST_MISS_E, LST_MISS_SLOT, LST_MISS_EV, LST_COLD, LST_NONCOLD, LST_COUNT };
 
@@ -70,6 +71,7 @@ struct PrepArgs {
   unsigned long long stride;         // bytes between experts / slots
   unsigned long long expert_bytes;
   int* err;
+  unsigned* seq_ctr;                 // per-handle prepare counter (stamps RecHdr.seq)
 };
 
 struct CopyArgs {
@@ -81,6 +83,7 @@ struct CopyArgs {
   uint8_t* scratch_base;
   unsigned long long stride;
   unsigned long long nvec;           // 16-byte vectors per expert
+  unsigned* ready;                   // [E] or null: ready[e] = RecHdr.seq once expert e is copied
 };
 
 struct MlpArgs {
@@ -116,6 +119,9 @@ cudaError_t launch_router(const float* logits, int T, int E, int k, int renorm,
 cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s);
 cudaError_t prepare_configure();   // kernel attributes, call outside capture
 cudaError_t launch_copy(const CopyArgs& a, int grid, cudaStream_t s);
+// Whole experts per CTA, each announced in a.ready once its bytes are written
+// (consumers poll the flag instead of waiting for the whole copy).
+cudaError_t launch_copy_flagged(const CopyArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_copy_raw(const void* src, void* dst, unsigned long long nvec, int grid,
                             cudaStream_t s);
 cudaError_t launch_verify(const int32_t* slot_expert, int N, const uint8_t* pool_base,
@@ -148,9 +154,16 @@ struct GemmBuffers {
   int32_t* order;          // [T*k]
   int4* tiles;             // [T*k]
   int* ntiles;             // [1]
+  unsigned* work;          // [2] item counters of the up / down GEMMs
   uint16_t* hb;            // [T*k, I] bf16
   float* out;              // [T*k, H] f32
   int* err;
+  // experts still being copied in this step: the up GEMM waits for
+  // ready[e] == hdr->seq before it reads an expert whose assignments are
+  // pending (null = everything is in place before the launch)
+  const uint8_t* pending;  // [T*k]
+  const unsigned* ready;   // [E]
+  const RecHdr* hdr;
 };
 bool moe_gemm_supported(int wdtype, int H, int I, int k);
 cudaError_t moe_gemm_configure(int wdtype);   // call outside capture

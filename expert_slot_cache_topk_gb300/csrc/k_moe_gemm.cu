@@ -59,6 +59,7 @@ struct GemmArgs {
   const int32_t* order;        // [n] assignment indices grouped by expert
   const int4* tiles;           // [ntiles] {first position in order, rows, expert, 0}
   const int* ntiles;
+  unsigned* work;              // [2] next item of the up / down GEMM (reset by k_group)
   const void* x;               // [T, H] bf16 activations (up)
   uint16_t* hb;                // [n, I] bf16 h (written by up, read by down)
   float* out;                  // [n, H] f32 rows, one per assignment (down)
@@ -67,6 +68,9 @@ struct GemmArgs {
   int k, H, I;
   unsigned long long off_w2, off_s13, off_s2;
   int* err;
+  const uint8_t* pending;      // [n] or null: assignment's expert is copied in this step
+  const unsigned* ready;       // [E]: ready[e] == hdr->seq once expert e has landed
+  const RecHdr* hdr;
 };
 
 // ------------------------------------------------------------- grouping
@@ -76,13 +80,14 @@ struct GemmArgs {
 // most kTileM.
 __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const int32_t* __restrict__ ids, int n, int E,
                                                             int32_t* __restrict__ order, int4* __restrict__ tiles,
-                                                            int* __restrict__ ntiles) {
+                                                            int* __restrict__ ntiles, unsigned* __restrict__ work) {
   __shared__ int cnt[MOE_MAX_EXPERTS];
   __shared__ int off[MOE_MAX_EXPERTS];
   __shared__ int toff[MOE_MAX_EXPERTS];
   __shared__ int cur[MOE_MAX_EXPERTS];
   __shared__ int wsum[2][kGroupThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < 2) work[tid] = 0u;   // item counters of the up and down GEMMs
   for (int e = tid; e < E; e += blockDim.x) {
     cnt[e] = 0;
     cur[e] = 0;
@@ -185,7 +190,6 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
   const int ntiles = *g.ntiles;
   const int NT = PH == PH_UP ? g.I / 64 : g.H / kTileN;
   const int items = ntiles * NT;
-  if ((int)blockIdx.x >= items) return;
   const int K = PH == PH_UP ? g.H : g.I;
   const int nk = K / (int)tc::kTileK;
   const size_t wrb = PH == PH_UP ? (F == MOE_BF16 ? (size_t)g.H * 2 : (size_t)g.H / 2)
@@ -209,7 +213,12 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
   const int hh = tid >> 7;             // which 32-element half of the K step this thread stages
   unsigned gs = 0;                     // K steps of this CTA so far (stage = gs % kGStagesP)
   bool dead = false;
-  for (int item = blockIdx.x; item < items && !dead; item += gridDim.x) {
+  // items are taken from a shared counter, so a CTA that starts late (its SM
+  // busy with another kernel) simply takes fewer of them
+  __shared__ int next_item;
+  if (tid == 0) next_item = (int)atomicAdd(g.work + PH, 1u);
+  __syncthreads();
+  for (int item = next_item; item < items && !dead; item = next_item) {
     const int tile = item / NT, nt = item - tile * NT;
     const int4 td = g.tiles[tile];
     const int pos0 = td.x, rows = td.y;
@@ -219,6 +228,22 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
       rows_idx[tid] = PH == PH_UP ? a / g.k : a;
     }
     __syncthreads();
+    if (PH == PH_UP && g.pending != nullptr && tid == 0 && g.pending[asg_of[0]] != 0) {
+      // the expert is being copied in this step: wait (bounded) until its copy is published
+      const unsigned want = g.hdr->seq;
+      const unsigned long long t0 = tc::global_ns();
+      for (unsigned it = 0;; ++it) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(g.ready + td.z) : "memory");
+        if (v == want) break;
+        if ((it & 63u) == 63u && tc::global_ns() - t0 > 2000000000ull) {
+          dead = true;
+          break;
+        }
+        __nanosleep(256);
+      }
+    }
+    if (__syncthreads_or(dead)) break;
     const unsigned long long blk = g.asg_ptr[asg_of[0]];
     const uint8_t* wb = reinterpret_cast<const uint8_t*>(blk) + (PH == PH_UP ? 0 : g.off_w2);
     const uint16_t* sbase = reinterpret_cast<const uint16_t*>(blk + (PH == PH_UP ? g.off_s13 : g.off_s2));
@@ -364,6 +389,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
                                    __uint_as_float(v1[4 * q + 2]), __uint_as_float(v1[4 * q + 3]));
       }
     }
+    if (tid == 0) next_item = (int)atomicAdd(g.work + PH, 1u);
     tc::fence_before_sync();
     __syncthreads();    // accumulator, tile tables and scales free for the next item
   }
@@ -454,13 +480,14 @@ template <int F>
 cudaError_t gemm_impl(const MlpArgs& a, const GemmBuffers& b, cudaStream_t s) {
   if (!GemmState<F>::configured || GemmState<F>::blocks_per_sm < 1) return cudaErrorNotSupported;
   const int n = a.T * a.k;
-  k_group<<<1, kGroupThreads, 0, s>>>(b.ids, n, b.E, b.order, b.tiles, b.ntiles);
+  k_group<<<1, kGroupThreads, 0, s>>>(b.ids, n, b.E, b.order, b.tiles, b.ntiles, b.work);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   GemmArgs g{};
   g.order = b.order;
   g.tiles = b.tiles;
   g.ntiles = b.ntiles;
+  g.work = b.work;
   g.x = a.x;
   g.hb = b.hb;
   g.out = b.out;
@@ -473,6 +500,9 @@ cudaError_t gemm_impl(const MlpArgs& a, const GemmBuffers& b, cudaStream_t s) {
   g.off_s13 = a.off_s13;
   g.off_s2 = a.off_s2;
   g.err = b.err;
+  g.pending = b.pending;
+  g.ready = b.ready;
+  g.hdr = b.hdr;
   const int grid = GemmState<F>::blocks_per_sm * dev_sms();
   k_moe_gemm<F, PH_UP><<<grid, kGThreads, kGemmSmem, s>>>(g);
   e = cudaGetLastError();

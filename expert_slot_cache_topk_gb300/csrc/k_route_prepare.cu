@@ -59,6 +59,43 @@ __global__ void __launch_bounds__(kCopyThreads) k_copy(CopyArgs a) {
   }
 }
 
+// Same copies, one whole expert per CTA at a time, in list order (ascending
+// expert id); once an expert's bytes are written the CTA publishes
+// ready[e] = hdr->seq, so a consumer can start on that expert while later
+// ones are still in flight.
+__global__ void __launch_bounds__(kCopyThreads) k_copy_flagged(CopyArgs a) {
+  const RecHdr h = *a.hdr;
+  const int n = h.bypass ? h.n_noncold : h.n_misses;
+  const int32_t* src_list = a.lists + (h.bypass ? LST_NONCOLD : LST_MISS_E) * a.E;
+  const int32_t* slot_list = a.lists + LST_MISS_SLOT * a.E;
+  for (int which = blockIdx.x; which < n; which += gridDim.x) {
+    const int e = src_list[which];
+    const uint4* src = reinterpret_cast<const uint4*>(a.host_base + (unsigned long long)e * a.stride);
+    uint8_t* dst_b = h.bypass ? a.scratch_base + (unsigned long long)which * a.stride
+                              : a.pool_base + (unsigned long long)slot_list[which] * a.stride;
+    uint4* dst = reinterpret_cast<uint4*>(dst_b);
+    for (unsigned long long base = threadIdx.x; base < a.nvec; base += (unsigned long long)kCopyChunkVec) {
+      uint4 v[kCopyVecPerThread];
+#pragma unroll
+      for (int u = 0; u < kCopyVecPerThread; ++u) {
+        const unsigned long long i = base + (unsigned long long)u * kCopyThreads;
+        if (i < a.nvec) v[u] = __ldcs(src + i);
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyVecPerThread; ++u) {
+        const unsigned long long i = base + (unsigned long long)u * kCopyThreads;
+        if (i < a.nvec) dst[i] = v[u];
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a.ready + e), "r"(h.seq) : "memory");
+    }
+  }
+}
+
 // Plain copy of nvec 16-byte vectors (used to time the UVA path at create).
 __global__ void __launch_bounds__(kCopyThreads) k_copy_raw(const uint4* __restrict__ src,
                                                            uint4* __restrict__ dst,
@@ -129,7 +166,7 @@ cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s) {
 // L1 / shared-memory split in between.
 cudaError_t prepare_configure() {
   const void* kernels[] = {(const void*)k_router, (const void*)k_prepare<256>, (const void*)k_prepare<kPrepThreads>,
-                           (const void*)k_copy};
+                           (const void*)k_copy, (const void*)k_copy_flagged};
   for (const void* k : kernels) {
     const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                                (int)cudaSharedmemCarveoutMaxShared);
@@ -140,6 +177,11 @@ cudaError_t prepare_configure() {
 
 cudaError_t launch_copy(const CopyArgs& a, int grid, cudaStream_t s) {
   k_copy<<<grid, kCopyThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_flagged(const CopyArgs& a, int grid, cudaStream_t s) {
+  k_copy_flagged<<<grid, kCopyThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

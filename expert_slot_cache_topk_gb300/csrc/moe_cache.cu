@@ -69,6 +69,8 @@ struct moe_cache {
   int4* tiles_d = nullptr;        //               tiles of up to 128 assignments
   int* ntiles_d = nullptr;
   float* gout_d = nullptr;        //               [T*k, H] f32 per-assignment outputs
+  unsigned* seq_d = nullptr;      // prepare counter (RecHdr.seq)
+  unsigned* ready_d = nullptr;    // [E] expert e copied in the step with that seq
   std::vector<uint8_t> cold_h;
   bool any_cold = false;
   uint8_t* pool_d = nullptr;
@@ -97,6 +99,7 @@ struct moe_cache {
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_sync = nullptr;
   int copy_mode = MOE_COPY_UVA;
   int copy_grid = 0;
+  int flag_grid = 0;              // CTAs of the flagged (overlapped) copy: enough to fill the host link
   double memcpy_gbs = 0, uva_gbs = 0;
   unsigned long long launches = 0;
   bool timing_on = false;
@@ -224,6 +227,7 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
   a.stride = c->stride;
   a.expert_bytes = c->Be;
   a.err = c->err_d;
+  a.seq_ctr = c->seq_d;
   const int ti = tm_begin(c, TM_ROUTE, s);
   if (logits) {
     a.w_out = c->w_d;
@@ -249,7 +253,8 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
 // shape allows it; else the cooperative up/down kernel.  `*launches` = the
 // kernels launched.  cudaErrorNotSupported (or a too-large cooperative grid)
 // = none fits; the caller then runs the separate up and down kernels.
-cudaError_t launch_layer_mlp(moe_cache* c, const MlpArgs& m, cudaStream_t s, int* launches) {
+cudaError_t launch_layer_mlp(moe_cache* c, const MlpArgs& m, cudaStream_t s, int* launches,
+                             int overlap_layer = -1) {
   *launches = 1;
   if (c->staged_mlp && m.T == 1) {
     const cudaError_t e = launch_mlp_ring(c->wd, m, c->bar_d, c->err_d, s);
@@ -262,9 +267,15 @@ cudaError_t launch_layer_mlp(moe_cache* c, const MlpArgs& m, cudaStream_t s, int
     b.order = c->order_d;
     b.tiles = c->tiles_d;
     b.ntiles = c->ntiles_d;
+    b.work = reinterpret_cast<unsigned*>(c->ntiles_d + 2);
     b.hb = reinterpret_cast<uint16_t*>(c->h_d);
     b.out = c->gout_d;
     b.err = c->err_d;
+    if (overlap_layer >= 0) {
+      b.pending = c->pend_d;
+      b.ready = c->ready_d;
+      b.hdr = c->hdr_d + overlap_layer;
+    }
     const cudaError_t e = launch_moe_gemm(c->wd, m, b, s);
     if (e != cudaErrorNotSupported) {
       *launches = 4;
@@ -308,6 +319,53 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
     // no co-resident grid for this shape: copy kernel, then the MLP
   }
   const bool memcpy_mode = c->copy_mode == MOE_COPY_MEMCPY;
+  if (mlp != nullptr && mlp->T > 1 && c->gemm_mlp && !memcpy_mode) {
+    // Multi-token step on the tensor cores: the copy kernel publishes every
+    // expert as it lands and the grouped GEMM starts on the first ones while
+    // later ones are still crossing the host link; the caller's stream joins
+    // the copy stream after the MLP.
+    CK(c, cudaEventRecord(c->ev_fork, s));
+    CK(c, cudaStreamWaitEvent(c->copy_stream, c->ev_fork, 0));
+    int ti = tm_begin(c, TM_COPY, c->copy_stream);
+    CopyArgs a{};
+    a.hdr = c->hdr_d + layer;
+    a.lists = c->lists_d + (size_t)layer * LST_COUNT * c->E;
+    a.E = c->E;
+    a.host_base = c->backing_dv + (size_t)layer * c->E * c->stride;
+    a.pool_base = pool;
+    a.scratch_base = c->scratch_d;
+    a.stride = c->stride;
+    a.nvec = c->nvec;
+    a.ready = c->ready_d;
+    CK(c, launch_copy_flagged(a, c->flag_grid, c->copy_stream));
+    c->launches++;
+    tm_end(c, TM_COPY, ti, c->copy_stream);
+    CK(c, cudaEventRecord(c->ev_join, c->copy_stream));
+    ti = tm_begin(c, TM_UP, s);
+    int nl = 1;
+    const cudaError_t fe = launch_layer_mlp(c, *mlp, s, &nl, layer);
+    if (fe == cudaSuccess) {
+      c->launches += nl;
+      tm_end(c, TM_UP, ti, s);
+      CK(c, cudaStreamWaitEvent(s, c->ev_join, 0));
+      return MOE_OK;
+    }
+    if (fe != cudaErrorNotSupported && fe != cudaErrorCooperativeLaunchTooLarge)
+      return cuda_fail(c, fe, "grouped expert MLP launch");
+    cudaGetLastError();
+    tm_end(c, TM_UP, ti, s);
+    // the grouped GEMM could not be launched: join, then the per-token kernels
+    CK(c, cudaStreamWaitEvent(s, c->ev_join, 0));
+    ti = tm_begin(c, TM_UP, s);
+    CK(c, launch_mlp_up(c->wd, *mlp, s));
+    c->launches++;
+    tm_end(c, TM_UP, ti, s);
+    ti = tm_begin(c, TM_DOWN, s);
+    CK(c, launch_mlp_down(c->wd, *mlp, s));
+    c->launches++;
+    tm_end(c, TM_DOWN, ti, s);
+    return MOE_OK;
+  }
   if (memcpy_mode && capturing(s))
     return fail(c, MOE_ESTATE, "MOE_COPY_MEMCPY needs a host decision per step and cannot be captured; use MOE_COPY_UVA");
   CK(c, cudaEventRecord(c->ev_fork, s));
@@ -457,7 +515,7 @@ void free_all(moe_cache* c) {
   void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->slot_map_d, c->slot_expert_d,
                  c->slot_stamp_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
                  c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->tm_miss_d, c->xs_d[0], c->xs_d[1],
-                 c->logits_stage_d, c->order_d, c->tiles_d, c->ntiles_d, c->gout_d};
+                 c->logits_stage_d, c->order_d, c->tiles_d, c->ntiles_d, c->gout_d, c->seq_d, c->ready_d};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->backing_h) cudaFreeHost(c->backing_h);
@@ -620,6 +678,12 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   CKC(dmalloc((void**)&c->h_d, TK * c->I * sizeof(float)));
   CKC(dmalloc((void**)&c->err_d, sizeof(int)));
   CKC(dmalloc((void**)&c->bar_d, sizeof(GridBar)));
+  CKC(dmalloc((void**)&c->seq_d, sizeof(unsigned)));
+  CKC(dmalloc((void**)&c->ready_d, (size_t)E * sizeof(unsigned)));
+  // zeroed once: the prepare counter never goes back (not even on reset), so
+  // a ready flag left by an earlier step can never match a later step
+  CKC(cudaMemset(c->seq_d, 0, sizeof(unsigned)));
+  CKC(cudaMemset(c->ready_d, 0, (size_t)E * sizeof(unsigned)));
   CKC(dmalloc((void**)&c->verify_d, sizeof(int)));
   CKC(dmalloc((void**)&c->xs_d[0], (size_t)c->maxT * c->H * act_bytes(c->wd)));
   CKC(dmalloc((void**)&c->xs_d[1], (size_t)c->maxT * c->H * act_bytes(c->wd)));
@@ -639,7 +703,7 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   if (c->staged_mlp && c->maxT > 1 && moe_gemm_supported(c->wd, c->H, c->I, c->K)) {
     CKC(dmalloc((void**)&c->order_d, TK * sizeof(int32_t)));
     CKC(dmalloc((void**)&c->tiles_d, TK * sizeof(int4)));
-    CKC(dmalloc((void**)&c->ntiles_d, sizeof(int)));
+    CKC(dmalloc((void**)&c->ntiles_d, 4 * sizeof(int)));   // tile count + two item counters
     CKC(dmalloc((void**)&c->gout_d, TK * c->H * sizeof(float)));
     CKC(moe_gemm_configure(c->wd));
     c->gemm_mlp = true;
@@ -647,6 +711,7 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   int sms = 0;
   CKC(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, g.device));
   c->copy_grid = std::max(1, sms) * 4;
+  c->flag_grid = std::max(1, std::min(64, sms / 2));
   c->copy_mode = g.copy_mode;
   if (g.copy_mode == MOE_COPY_AUTO) {
     if (measure_copy_modes(c) != MOE_OK) return bail(MOE_ECUDA);

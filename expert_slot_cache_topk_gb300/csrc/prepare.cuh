@@ -211,6 +211,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
       atomicExch(a.err, DEVERR_BAD_ID);
       RecHdr h = {};
       h.n_ids = n_ids;
+      h.seq = a.seq_ctr ? atomicAdd(a.seq_ctr, 1u) + 1u : 0u;
       *a.hdr = h;
     }
     for (int i = tid; i < n_ids; i += nthr) {
@@ -320,6 +321,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
     h.n_hits = nh;
     h.n_misses = nm;
     h.n_evictions = nvict;
+    h.seq = a.seq_ctr ? atomicAdd(a.seq_ctr, 1u) + 1u : 0u;
     *a.hdr = h;
   }
 
