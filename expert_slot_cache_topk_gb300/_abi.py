@@ -38,13 +38,15 @@ class moe_cache_config(C.Structure):
                 ("hidden", C.c_int), ("inter", C.c_int), ("wdtype", C.c_int),
                 ("slots_per_layer", C.c_int), ("max_tokens", C.c_int), ("renormalize", C.c_int),
                 ("cold_mask_h", C.POINTER(C.c_uint8)), ("copy_mode", C.c_int), ("device", C.c_int),
-                ("hbm_budget_bytes", C.c_size_t), ("mlp_kernel", C.c_int)]
+                ("hbm_budget_bytes", C.c_size_t), ("mlp_kernel", C.c_int),
+                ("move_interval", C.c_int), ("move_decay", C.c_float), ("move_threshold", C.c_float),
+                ("move_count_tokens", C.c_int)]
 
 
 class moe_cache_counters(C.Structure):
     _fields_ = [(n, C.c_uint64) for n in ("steps", "hits", "misses", "evictions", "bypass_steps",
                                           "cold_reads", "bytes_h2d_miss", "bytes_h2d_bypass",
-                                          "bytes_uva_cold")]
+                                          "bytes_uva_cold", "moves")]
 
 
 class moe_prepare_info(C.Structure):
@@ -94,6 +96,7 @@ SIGNATURES = {
     "moe_cache_stats": (_S, [_H, _I, C.POINTER(moe_cache_counters)]),
     "moe_cache_get_state": (_S, [_H, _I, _P, _P, _P, _P]),
     "moe_cache_verify_slots": (_S, [_H, _I, C.POINTER(_I)]),
+    "moe_cache_get_cold": (_S, [_H, _I, _P]),
     "moe_cache_pool_ptrs": (_S, [_H, _I, C.POINTER(_P), C.POINTER(_P)]),
     "moe_cache_check": (_S, [_H]),
     "moe_cache_reset": (_S, [_H]),
@@ -180,7 +183,9 @@ class MoECache:
 
     def __init__(self, num_layers, num_experts, top_k, hidden, inter, wdtype, slots, max_tokens,
                  renormalize=False, cold_mask=None, copy_mode="uva", device=0, hbm_budget_bytes=0,
-                 mlp_kernel="auto"):
+                 mlp_kernel="auto", moves=None):
+        """moves: None (off) or a dict with interval, decay, threshold, count_tokens
+        (run-time moves between the cold set and the pool; see moe_cache_config)."""
         self.L, self.E, self.k, self.H, self.I = num_layers, num_experts, top_k, hidden, inter
         self.wdtype, self.N, self.max_tokens = wdtype, slots, max_tokens
         cfg = moe_cache_config()
@@ -197,6 +202,11 @@ class MoECache:
         cfg.device = device
         cfg.hbm_budget_bytes = hbm_budget_bytes
         cfg.mlp_kernel = MLP_KERNEL[mlp_kernel]
+        if moves:
+            cfg.move_interval = int(moves.get("interval", 8))
+            cfg.move_decay = float(moves.get("decay", 2.0 ** (-1.0 / 64.0)))
+            cfg.move_threshold = float(moves.get("threshold", 2.0))
+            cfg.move_count_tokens = int(moves.get("count_tokens", 1))
         h = _H()
         _check(lib().moe_cache_create(C.byref(cfg), C.byref(h)))
         self._h = h
@@ -294,6 +304,12 @@ class MoECache:
         n = C.c_int()
         self._ck(lib().moe_cache_verify_slots(self._h, layer, C.byref(n)))
         return n.value
+
+    def get_cold(self, layer: int) -> np.ndarray:
+        """Current cold set of a layer (bool [E])."""
+        m = np.zeros(self.E, np.uint8)
+        self._ck(lib().moe_cache_get_cold(self._h, layer, m.ctypes.data))
+        return m.astype(bool)
 
     def pool_ptrs(self, layer: int):
         p, s = _P(), _P()

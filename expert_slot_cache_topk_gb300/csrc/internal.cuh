@@ -17,13 +17,13 @@ constexpr int kCopyChunkVec = kCopyThreads * kCopyVecPerThread;  // 32 KiB per C
 // Per-layer counters and LRU clock, device resident.
 enum {
   ST_STEPS = 0, ST_HITS, ST_MISSES, ST_EVICT, ST_BYPASS, ST_COLD,
-  ST_B_MISS, ST_B_BYPASS, ST_B_COLD, ST_COUNT
+  ST_B_MISS, ST_B_BYPASS, ST_B_COLD, ST_MOVES, ST_COUNT
 };
 
 struct LayerState {
   unsigned long long clock;   // next recency stamp
-  int nfree;                  // free slots are exactly [0, nfree)
-  int pad;
+  int nfree;                  // free slots: free_stack[0 .. nfree), the next miss takes the last
+  unsigned counted;           // steps counted for run-time moves
   unsigned long long stats[ST_COUNT];
 };
 
@@ -54,7 +54,12 @@ struct PrepArgs {
   // ids [T*k] (read; written first when do_route)
   int32_t* ids;
   int T, k, E, N;
-  const uint8_t* cold;               // [E] of this layer, may be null
+  uint8_t* cold;                     // [E] of this layer, may be null (updated by run-time moves)
+  int32_t* free_stack;               // [N] of this layer
+  float* counts;                     // [E] of this layer: use counts for run-time moves
+  int move_interval;                 // 0 = no run-time moves
+  int move_count_tokens;
+  float move_decay, move_threshold;
   int32_t* slot_map;                 // [E]
   int32_t* slot_expert;              // [N]
   long long* slot_stamp;             // [N]

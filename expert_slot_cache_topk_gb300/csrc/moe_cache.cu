@@ -76,6 +76,8 @@ struct moe_cache {
   uint8_t* pool_d = nullptr;
   uint8_t* scratch_d = nullptr;
   uint8_t* cold_d = nullptr;
+  int32_t* fstack_d = nullptr;    // [L][N] free-slot stacks
+  float* counts_d = nullptr;      // [L][E] use counts for run-time moves (null when off)
   int32_t* slot_map_d = nullptr;
   int32_t* slot_expert_d = nullptr;
   long long* slot_stamp_d = nullptr;
@@ -211,6 +213,14 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
   a.N = c->N;
   a.renorm = c->cfg.renormalize;
   a.cold = c->any_cold ? c->cold_d + (size_t)layer * c->E : nullptr;
+  a.free_stack = c->fstack_d + (size_t)layer * c->N;
+  if (c->counts_d != nullptr && c->any_cold) {
+    a.counts = c->counts_d + (size_t)layer * c->E;
+    a.move_interval = c->cfg.move_interval;
+    a.move_count_tokens = c->cfg.move_count_tokens;
+    a.move_decay = c->cfg.move_decay;
+    a.move_threshold = c->cfg.move_threshold;
+  }
   a.slot_map = c->slot_map_d + (size_t)layer * c->E;
   a.slot_expert = c->slot_expert_d + (size_t)layer * c->N;
   a.slot_stamp = c->slot_stamp_d + (size_t)layer * c->N;
@@ -512,7 +522,7 @@ void free_all(moe_cache* c) {
   if (c->ev_join) cudaEventDestroy(c->ev_join);
   if (c->ev_sync) cudaEventDestroy(c->ev_sync);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
-  void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->slot_map_d, c->slot_expert_d,
+  void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->fstack_d, c->counts_d, c->slot_map_d, c->slot_expert_d,
                  c->slot_stamp_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
                  c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->tm_miss_d, c->xs_d[0], c->xs_d[1],
                  c->logits_stage_d, c->order_d, c->tiles_d, c->ntiles_d, c->gout_d, c->seq_d, c->ready_d};
@@ -531,6 +541,15 @@ moe_status init_state(moe_cache* c) {
     CK(c, cudaMemset(c->slot_expert_d, 0xFF, L * N * sizeof(int32_t)));
     CK(c, cudaMemset(c->slot_stamp_d, 0, L * N * sizeof(long long)));
   }
+  if (N) {
+    std::vector<int32_t> fs(L * N);
+    for (size_t l = 0; l < L; ++l)
+      for (size_t i = 0; i < N; ++i) fs[l * N + i] = (int32_t)i;   // the first miss takes slot N - 1
+    CK(c, cudaMemcpy(c->fstack_d, fs.data(), fs.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  }
+  // the cold set given at create (run-time moves change it) and zero use counts
+  CK(c, cudaMemcpy(c->cold_d, c->cold_h.data(), L * E, cudaMemcpyHostToDevice));
+  if (c->counts_d) CK(c, cudaMemset(c->counts_d, 0, L * E * sizeof(float)));
   std::vector<LayerState> st(L);
   for (auto& s : st) {
     memset(&s, 0, sizeof(s));
@@ -590,6 +609,10 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   if (g.copy_mode < MOE_COPY_AUTO || g.copy_mode > MOE_COPY_FUSED)
     return fail(nullptr, MOE_EINVAL, "bad copy_mode");
   if (g.renormalize != 0 && g.renormalize != 1) return fail(nullptr, MOE_EINVAL, "renormalize must be 0 or 1");
+  if (g.move_interval < 0) return fail(nullptr, MOE_EINVAL, "move_interval must be >= 0");
+  if (g.move_interval > 0 && (!(g.move_decay > 0.f && g.move_decay <= 1.f) || !(g.move_threshold >= 0.f) ||
+                              !(g.move_threshold < 3.0e38f) || g.move_count_tokens < 1))
+    return fail(nullptr, MOE_EINVAL, "moves need 0 < move_decay <= 1, finite move_threshold >= 0, move_count_tokens >= 1");
   if (mlp_up_smem_bytes(g.hidden) > 200 * 1024 || mlp_down_smem_bytes(g.top_k, g.inter) > 200 * 1024)
     return fail(nullptr, MOE_EINVAL, "hidden*4 and top_k*inter*4 must each fit in 200 KiB of shared memory");
   int ndev = 0;
@@ -667,6 +690,8 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   CKC(dmalloc((void**)&c->slot_map_d, L * E * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->slot_expert_d, L * N * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->slot_stamp_d, L * N * sizeof(long long)));
+  CKC(dmalloc((void**)&c->fstack_d, (L * N > 0 ? L * N : 1) * sizeof(int32_t)));
+  if (g.move_interval > 0) CKC(dmalloc((void**)&c->counts_d, L * E * sizeof(float)));
   CKC(dmalloc((void**)&c->state_d, L * sizeof(LayerState)));
   CKC(dmalloc((void**)&c->hdr_d, L * sizeof(RecHdr)));
   CKC(dmalloc((void**)&c->lists_d, L * LST_COUNT * E * sizeof(int32_t)));
@@ -919,6 +944,7 @@ moe_status moe_cache_stats(moe_cache_t* c, int layer, moe_cache_counters* out) {
   out->bytes_h2d_miss = acc[ST_B_MISS];
   out->bytes_h2d_bypass = acc[ST_B_BYPASS];
   out->bytes_uva_cold = acc[ST_B_COLD];
+  out->moves = acc[ST_MOVES];
   return device_error(c);
 }
 
@@ -960,6 +986,16 @@ moe_status moe_cache_verify_slots(moe_cache_t* c, int layer, int* mismatched_slo
   CK(c, cudaDeviceSynchronize());
   CK(c, cudaMemcpy(mismatched_slots, c->verify_d, sizeof(int), cudaMemcpyDeviceToHost));
   return MOE_OK;
+}
+
+moe_status moe_cache_get_cold(moe_cache_t* c, int layer, uint8_t* cold_h) {
+  moe_status st = check_layer(c, layer);
+  if (st != MOE_OK) return st;
+  if (!cold_h) return fail(c, MOE_EINVAL, "null buffer");
+  CK(c, cudaSetDevice(c->cfg.device));
+  CK(c, cudaDeviceSynchronize());
+  CK(c, cudaMemcpy(cold_h, c->cold_d + (size_t)layer * c->E, c->E, cudaMemcpyDeviceToHost));
+  return device_error(c);
 }
 
 moe_status moe_cache_pool_ptrs(moe_cache_t* c, int layer, void** pool_d, void** scratch_d) {

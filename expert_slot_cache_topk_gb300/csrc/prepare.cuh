@@ -157,13 +157,40 @@ struct PrepSmem {
   int sexp[MOE_MAX_EXPERTS];       // slot -> expert (-1 free)
   long long stamp[MOE_MAX_EXPERTS];
   int victim[MOE_MAX_EXPERTS];
-  unsigned char mark[MOE_MAX_EXPERTS];
+  int nsel[MOE_MAX_EXPERTS];             // assignments of each expert in this step
+  int fstack[MOE_MAX_EXPERTS];           // free-slot stack (the next miss takes fstack[nfree - 1])
+  float counts[MOE_MAX_EXPERTS];         // use counts for run-time moves
+  unsigned long long red[2][32];         // block reductions of the move decision
   unsigned char newf[MOE_MAX_EXPERTS];   // expert copied in this step
   unsigned long long stats[ST_COUNT];    // the layer's counters, read at the start
   unsigned char cold[MOE_MAX_EXPERTS];
   int32_t ids[kMaxRoutedIds];
   int bad;
 };
+
+// Max (is_max) or min of one 64-bit value per thread over the CTA; every
+// thread must call it; the result is valid in thread 0.  buf holds 32 words.
+__device__ __forceinline__ unsigned long long block_reduce_u64(unsigned long long v, bool is_max,
+                                                               unsigned long long* buf) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(kFullMask, v, o);
+    v = is_max ? (w > v ? w : v) : (w < v ? w : v);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = (blockDim.x + 31) >> 5;
+  __syncthreads();
+  if (lane == 0) buf[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < nw ? buf[lane] : (is_max ? 0ull : ~0ull);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long w = __shfl_xor_sync(kFullMask, v, o);
+      v = is_max ? (w > v ? w : v) : (w < v ? w : v);
+    }
+  }
+  return v;
+}
 
 // One layer step's bookkeeping by the calling CTA (blockDim.x >= E, a multiple
 // of 32; do_route needs T <= 64).
@@ -181,15 +208,19 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
   const unsigned long long clk = a.st->clock;
   const int nfree = a.st->nfree;
   const int l0 = (a.do_route && nthr >= 32 * a.T + 32) ? 32 * a.T : 0;   // first state-loading thread
+  const bool moving = a.move_interval > 0 && a.counts != nullptr && a.T <= a.move_count_tokens;
+  const unsigned counted = moving ? a.st->counted + 1u : 0u;
   for (int q = tid - l0; q >= 0 && q < E; q += nthr - l0) {
     S.map[q] = a.slot_map[q];
     S.cold[q] = a.cold != nullptr ? a.cold[q] : 0;
-    S.mark[q] = 0;
+    S.nsel[q] = 0;
     S.newf[q] = 0;
+    if (moving) S.counts[q] = a.counts[q];
   }
   for (int q = tid - l0; q >= 0 && q < N; q += nthr - l0) {
     S.sexp[q] = a.slot_expert[q];
     S.stamp[q] = a.slot_stamp[q];
+    S.fstack[q] = a.free_stack[q];
   }
   if (tid - l0 >= 0 && tid - l0 < ST_COUNT) S.stats[tid - l0] = a.st->stats[tid - l0];
   if (tid == 0) S.bad = 0;
@@ -202,7 +233,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
   for (int i = tid; i < n_ids; i += nthr) {
     const int e = ids_in_smem ? S.ids[i] : a.ids[i];
     if ((unsigned)e >= (unsigned)E) S.bad = 1;
-    else S.mark[e] = 1;
+    else atomicAdd(&S.nsel[e], 1);
   }
   __syncthreads();
   if (S.bad) {
@@ -224,7 +255,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
   }
 
   const int e = tid;
-  const int sel = (e < E) ? S.mark[e] : 0;
+  const int sel = (e < E) ? (S.nsel[e] > 0) : 0;
   const int cold = sel && S.cold[e];
   const int nc = sel && !cold;
   const int hit = nc && S.map[e] >= 0;
@@ -264,7 +295,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
     int slot = -1, ev = -1;
     if (miss) {
       if (r_m < nfree) {
-        slot = nfree - 1 - r_m;                // free list [0, nfree), popped from the end
+        slot = S.fstack[nfree - 1 - r_m];      // free-slot stack, popped from the end
       } else {
         slot = S.victim[r_m - nfree];          // i-th least recently used slot
         ev = S.sexp[slot];
@@ -346,6 +377,52 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
     if (a.asg_ptr) a.asg_ptr[i] = p;
     if (a.src_ptr) a.src_ptr[i] = host;
     if (a.pending) a.pending[i] = S.newf[x];
+  }
+
+  // Run-time moves between the cold set and the pool, after the step's own
+  // bookkeeping ("Running 125B MoE on Two 32 GB Cards", section 4.4: decayed
+  // use counts, the most used host expert and the least used GPU-side expert
+  // trade places).  float32 with explicit rounding, as the oracle does.
+  if (moving) {
+    float cnt = 0.f;
+    if (e < E) {
+      cnt = S.counts[e];
+      if (S.nsel[e] > 0) cnt = __fadd_rn(cnt, (float)S.nsel[e]);
+    }
+    const bool decide = counted % (unsigned)a.move_interval == 0u;
+    if (decide && e < E) cnt = __fmul_rn(cnt, a.move_decay);
+    if (e < E) a.counts[e] = cnt;
+    if (decide) {
+      // counts are >= 0, so their bits order like the values; ties to the lower id
+      unsigned long long kc = 0ull, kh = ~0ull;
+      if (e < E) {
+        const unsigned long long fb = (unsigned long long)__float_as_uint(cnt) << 32;
+        if (S.cold[e]) kc = fb | (0xFFFFFFFFull - (unsigned)e);
+        else kh = fb | (unsigned)e;
+      }
+      kc = block_reduce_u64(kc, true, S.red[0]);
+      kh = block_reduce_u64(kh, false, S.red[1]);
+      if (tid == 0 && kc != 0ull && kh != ~0ull) {
+        const int c = (int)(0xFFFFFFFFull - (kc & 0xFFFFFFFFull));
+        const int h = (int)(kh & 0xFFFFFFFFull);
+        const float fc = __uint_as_float((unsigned)(kc >> 32)), fh = __uint_as_float((unsigned)(kh >> 32));
+        if (__fsub_rn(fc, fh) > a.move_threshold) {
+          a.cold[c] = 0;
+          a.cold[h] = 1;
+          const int slot = S.map[h];
+          if (slot >= 0) {
+            // h leaves the pool: its slot goes on top of the free-slot stack
+            const int nf = bypass ? nfree : nfree - (nm < nfree ? nm : nfree);
+            a.slot_map[h] = -1;
+            a.slot_expert[slot] = -1;
+            a.free_stack[nf] = slot;
+            a.st->nfree = nf + 1;
+          }
+          atomicAdd(&a.st->stats[ST_MOVES], 1ull);
+        }
+      }
+    }
+    if (tid == 0) a.st->counted = counted;
   }
 }
 

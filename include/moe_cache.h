@@ -143,6 +143,20 @@ typedef struct {
   int device;            /* CUDA device ordinal */
   size_t hbm_budget_bytes; /* cap on pool + scratch bytes; 0 = half of free device memory */
   int mlp_kernel;        /* moe_mlp_kernel */
+  /* Run-time moves between the cold set and the pool ([Flash-Next 2x32GB]
+   * sections 4.3-4.4).  Steps with at most move_count_tokens tokens add each
+   * expert's number of assignments to a per-layer float32 use count; every
+   * move_interval such steps the counts are multiplied by move_decay, and if
+   * (largest count of a cold expert) - (smallest count of a non-cold expert)
+   * > move_threshold, the two trade places (ties to the lower id): the cold
+   * one is copied into a slot at its next use, the other is read in place from
+   * then on and its slot, if it held one, is freed.  move_interval = 0: off
+   * (the cold set never changes).  The pages' values: interval 8, decay
+   * 2^(-1/64) (half-life 512 steps), threshold 2, count tokens 1. */
+  int move_interval;
+  float move_decay;      /* (0, 1] */
+  float move_threshold;  /* >= 0 */
+  int move_count_tokens; /* >= 1 */
 } moe_cache_config;
 
 /* Cumulative per-layer counters (moe_cache_stats with layer = -1 sums layers).
@@ -158,6 +172,7 @@ typedef struct {
   uint64_t bytes_h2d_miss;   /* misses * expert bytes */
   uint64_t bytes_h2d_bypass; /* sum over bypass steps of D * expert bytes */
   uint64_t bytes_uva_cold;   /* cold_reads * expert bytes */
+  uint64_t moves;            /* run-time moves between the cold set and the pool */
 } moe_cache_counters;
 
 /* Result of the last prepare of one layer (moe_cache_last_prepare).
@@ -329,6 +344,10 @@ moe_status moe_cache_get_state(moe_cache_t* c, int layer, int32_t* slot_map_h,
  * ([vLLM #37190] "Test results": test_gpu_buffer_matches_source_weights).
  * Synchronises the device. */
 moe_status moe_cache_verify_slots(moe_cache_t* c, int layer, int* mismatched_slots);
+
+/* Current cold set of one layer (it changes only with run-time moves):
+ * cold_h[E] host buffer, 1 = cold.  Synchronises the device. */
+moe_status moe_cache_get_cold(moe_cache_t* c, int layer, uint8_t* cold_h);
 
 /* Device pointers of a layer's pool and of the bypass scratch. */
 moe_status moe_cache_pool_ptrs(moe_cache_t* c, int layer, void** pool_d, void** scratch_d);

@@ -69,30 +69,71 @@ class PrepareRecord:
     misses: list = field(default_factory=list)     # (expert, slot, evicted|-1), ascending expert
     copies: list = field(default_factory=list)     # (expert, dest index) in copy order
     slot_ids: np.ndarray = None                    # int32, same shape as topk_ids
+    move: tuple = None                             # (expert leaving the cold set, expert joining it,
+                                                   #  slot freed by the latter or -1), if a move happened
 
 
 STAT_KEYS = ("steps", "hits", "misses", "evictions", "bypass_steps", "cold_reads",
-             "bytes_h2d_miss", "bytes_h2d_bypass", "bytes_uva_cold")
+             "bytes_h2d_miss", "bytes_h2d_bypass", "bytes_uva_cold", "moves")
+
+
+@dataclass
+class MovePolicy:
+    """Run-time moves between the cold set and the pool ("Running 125B MoE on
+    Two 32 GB Cards", sections 4.3 "Moving experts at run time: simulation"
+    and 4.4 "... implementation": per-layer use counts from the decode router,
+    decayed, every few steps the most used host expert and the least used
+    GPU-side expert trade places when their counts differ by more than a
+    threshold, one pair per layer).
+
+    Readings taken here:
+    * a step is counted when it has at most ``count_tokens`` tokens (the pages
+      count decode steps and not prefill; decode there is batch 1);
+    * a counted step adds, to each expert, the number of its assignments in
+      that step, in one float32 addition;
+    * every ``interval`` counted steps, after the step's bookkeeping: the counts
+      are multiplied by ``decay`` (float32; 0.5 ** (8 / 512) = 2 ** (-1/64) for
+      the pages' interval 8 and half-life 512), then c = the cold expert with
+      the largest count and h = the non-cold expert with the smallest count
+      (ties to the lower id); if float32(count[c] - count[h]) > threshold, c
+      leaves the cold set and h joins it;
+    * nothing is copied at the decision: c is copied into a slot at its next
+      use (an ordinary miss); if h holds a slot, the slot is freed (pushed on
+      the free-slot stack, so the next miss takes it first) and h is read in
+      place from then on;
+    * all count arithmetic is float32, as on the GPU, so the integer outcomes
+      (which experts move) are decided in the same precision.
+    """
+
+    interval: int = 8
+    decay: float = float(np.float32(2.0 ** (-1.0 / 64.0)))
+    threshold: float = 2.0
+    count_tokens: int = 1
 
 
 class LayerSlotCache:
     """One MoE layer's pool of ``slots`` expert slots."""
 
-    def __init__(self, num_experts: int, slots: int, expert_bytes: int = 0, cold_mask=None):
+    def __init__(self, num_experts: int, slots: int, expert_bytes: int = 0, cold_mask=None,
+                 moves: "MovePolicy | None" = None):
         if not 0 <= slots <= num_experts:
             raise ValueError("need 0 <= slots <= num_experts")
         self.E = num_experts
         self.N = slots
         self.B = expert_bytes
-        self.cold = (np.zeros(num_experts, dtype=bool) if cold_mask is None
-                     else np.asarray(cold_mask, dtype=bool).copy())
+        self.cold0 = (np.zeros(num_experts, dtype=bool) if cold_mask is None
+                      else np.asarray(cold_mask, dtype=bool).copy())
+        self.moves = moves
         self.reset()
 
     def reset(self):
         self.lru: "OrderedDict[int, None]" = OrderedDict()   # front = least recently used
         self.expert_to_slot: dict[int, int] = {}
-        self.free: list[int] = list(range(self.N))
+        self.free: list[int] = list(range(self.N))            # a stack: pop() from the end
         self.stats = {k: 0 for k in STAT_KEYS}
+        self.cold = self.cold0.copy()
+        self.counts = np.zeros(self.E, dtype=np.float32)
+        self.counted_steps = 0
 
     # -- views used by tests -------------------------------------------------
     def slot_map(self) -> np.ndarray:
@@ -169,4 +210,37 @@ class LayerSlotCache:
             else:
                 flat_out[i] = SLOT_POOL | self.expert_to_slot[e]
         rec.slot_ids = out
+        if self.moves is not None:
+            self._count_and_move(ids, rec)
         return rec
+
+    # -- run-time moves between the cold set and the pool ------------------------
+    def _count_and_move(self, ids: np.ndarray, rec: PrepareRecord):
+        mp = self.moves
+        tokens = ids.shape[0] if ids.ndim >= 2 else 1
+        if tokens > mp.count_tokens:
+            return
+        n_sel = np.bincount(ids.reshape(-1), minlength=self.E)
+        for e in np.nonzero(n_sel)[0]:
+            self.counts[e] = np.float32(self.counts[e] + np.float32(n_sel[e]))
+        self.counted_steps += 1
+        if self.counted_steps % mp.interval:
+            return
+        self.counts = (self.counts * np.float32(mp.decay)).astype(np.float32)
+        cold_ids = np.nonzero(self.cold)[0]
+        warm_ids = np.nonzero(~self.cold)[0]
+        if cold_ids.size == 0 or warm_ids.size == 0:
+            return
+        c = int(cold_ids[np.argmax(self.counts[cold_ids])])     # argmax / argmin: first = lowest id
+        h = int(warm_ids[np.argmin(self.counts[warm_ids])])
+        if not np.float32(self.counts[c] - self.counts[h]) > np.float32(mp.threshold):
+            return
+        self.cold[c] = False
+        self.cold[h] = True
+        freed = -1
+        if h in self.expert_to_slot:
+            freed = self.expert_to_slot.pop(h)
+            del self.lru[h]
+            self.free.append(freed)
+        self.stats["moves"] += 1
+        rec.move = (c, h, freed)
