@@ -73,6 +73,8 @@ class PrepareRecord:
                                                    #  slot freed by the latter or -1), if a move happened
 
 
+POLICIES = ("lru", "lfu", "fifo", "slru")
+
 STAT_KEYS = ("steps", "hits", "misses", "evictions", "bypass_steps", "cold_reads",
              "bytes_h2d_miss", "bytes_h2d_bypass", "bytes_uva_cold", "moves")
 
@@ -115,9 +117,12 @@ class LayerSlotCache:
     """One MoE layer's pool of ``slots`` expert slots."""
 
     def __init__(self, num_experts: int, slots: int, expert_bytes: int = 0, cold_mask=None,
-                 moves: "MovePolicy | None" = None):
+                 moves: "MovePolicy | None" = None, policy: str = "lru"):
         if not 0 <= slots <= num_experts:
             raise ValueError("need 0 <= slots <= num_experts")
+        if policy not in POLICIES:
+            raise ValueError(f"policy must be one of {POLICIES}")
+        self.policy = policy
         self.E = num_experts
         self.N = slots
         self.B = expert_bytes
@@ -127,7 +132,12 @@ class LayerSlotCache:
         self.reset()
 
     def reset(self):
-        self.lru: "OrderedDict[int, None]" = OrderedDict()   # front = least recently used
+        # lru: recency order (front = least recently used); fifo / lfu: insertion
+        # order; slru: unused (prob / prot hold the two segments)
+        self.lru: "OrderedDict[int, None]" = OrderedDict()
+        self.freq: dict[int, int] = {}                        # lfu: steps used since insertion
+        self.prob: "OrderedDict[int, None]" = OrderedDict()   # slru probationary, front = LRU
+        self.prot: "OrderedDict[int, None]" = OrderedDict()   # slru protected, front = LRU
         self.expert_to_slot: dict[int, int] = {}
         self.free: list[int] = list(range(self.N))            # a stack: pop() from the end
         self.stats = {k: 0 for k in STAT_KEYS}
@@ -177,9 +187,10 @@ class LayerSlotCache:
                 scratch_pos[e] = r
                 rec.copies.append((e, r))
         else:
+            step = set(rec.noncold)
             for e in rec.noncold:                      # hits first, ascending
                 if e in self.expert_to_slot:
-                    self.lru.move_to_end(e)
+                    self._touch(e)
                     rec.hits.append(e)
                     self.stats["hits"] += 1
             for e in rec.noncold:                      # then misses, ascending
@@ -189,11 +200,12 @@ class LayerSlotCache:
                 if self.free:
                     s = self.free.pop()
                 else:
-                    evicted, _ = self.lru.popitem(last=False)
+                    evicted = self._victim(step)
+                    self._remove(evicted)
                     s = self.expert_to_slot.pop(evicted)
                     self.stats["evictions"] += 1
                 self.expert_to_slot[e] = s
-                self.lru[e] = None
+                self._insert(e)
                 rec.misses.append((e, s, evicted))
                 rec.copies.append((e, s))
                 self.stats["misses"] += 1
@@ -213,6 +225,61 @@ class LayerSlotCache:
         if self.moves is not None:
             self._count_and_move(ids, rec)
         return rec
+
+    # -- eviction policies ---------------------------------------------------------
+    # vLLM PR #37190 (the review thread that added --moe-expert-cache-policy):
+    # lru = least recently used, lfu = least frequently used, fifo = insertion
+    # order, slru = two segments, probationary -> protected, a 20 % / 80 %
+    # split.  Readings: every policy keeps the hits-before-misses order, and
+    # an expert used in the current step is never the victim; lfu counts the
+    # steps an expert was used in since it was inserted, ties to the earliest
+    # inserted; slru's protected segment holds floor(0.8 N) experts, a hit on
+    # a probationary expert promotes it to the protected MRU end, overflow
+    # demotes the protected LRU expert to the probationary MRU end, and the
+    # victim is the probationary LRU expert (the protected LRU one when the
+    # probationary segment has no candidate).
+    def _touch(self, e: int):
+        if self.policy == "lru":
+            self.lru.move_to_end(e)
+        elif self.policy == "lfu":
+            self.freq[e] += 1
+        elif self.policy == "slru":
+            if e in self.prob:
+                del self.prob[e]
+                self.prot[e] = None
+                if len(self.prot) > (4 * self.N) // 5:
+                    k, _ = self.prot.popitem(last=False)
+                    self.prob[k] = None
+            else:
+                self.prot.move_to_end(e)
+
+    def _insert(self, e: int):
+        if self.policy == "slru":
+            self.prob[e] = None
+        else:
+            self.lru[e] = None
+            if self.policy == "lfu":
+                self.freq[e] = 1
+
+    def _remove(self, e: int):
+        if self.policy == "slru":
+            self.prob.pop(e, None)
+            self.prot.pop(e, None)
+        else:
+            del self.lru[e]
+            self.freq.pop(e, None)
+
+    def _victim(self, step: set) -> int:
+        if self.policy == "slru":
+            for seg in (self.prob, self.prot):
+                for e in seg:
+                    if e not in step:
+                        return e
+            raise AssertionError("no victim")
+        cands = [e for e in self.lru if e not in step]     # in recency / insertion order
+        if self.policy == "lfu":
+            return min(cands, key=lambda e: self.freq[e])    # first of the minimum = earliest inserted
+        return cands[0]
 
     # -- run-time moves between the cold set and the pool ------------------------
     def _count_and_move(self, ids: np.ndarray, rec: PrepareRecord):
@@ -240,7 +307,7 @@ class LayerSlotCache:
         freed = -1
         if h in self.expert_to_slot:
             freed = self.expert_to_slot.pop(h)
-            del self.lru[h]
+            self._remove(h)
             self.free.append(freed)
         self.stats["moves"] += 1
         rec.move = (c, h, freed)

@@ -208,14 +208,10 @@ class _SinglePass(LayerSlotCache):
 
 
 class _EvictMRU(LayerSlotCache):
-    def reset(self):
-        super().reset()
-        lru = self.lru
+    """Evicts the most recently used expert not used in this step."""
 
-        class _Flip(type(lru)):
-            def popitem(self, last=True):
-                return super().popitem(last=not last)
-        self.lru = _Flip()
+    def _victim(self, step):
+        return [e for e in self.lru if e not in step][-1]
 
 
 class _FreeLowestFirst(LayerSlotCache):
