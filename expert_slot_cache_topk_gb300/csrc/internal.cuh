@@ -63,6 +63,8 @@ struct PrepArgs {
   int32_t* slot_map;                 // [E]
   int32_t* slot_expert;              // [N]
   long long* slot_stamp;             // [N]
+  int32_t* slot_aux;                 // [N]: LFU steps used, SLRU segment (1 = protected)
+  int policy;                        // moe_evict_policy
   LayerState* st;
   RecHdr* hdr;
   int32_t* lists;                    // [LST_COUNT * E]

@@ -1,6 +1,6 @@
 // Router, prepare, miss/bypass copy and slot verification kernels for
 // sm_103a.  The router and the per-layer slot bookkeeping live in
-// prepare.cuh (shared with the fused per-layer kernel).
+// prepare.cuh.
 
 #include <climits>
 #include <cstdint>
@@ -22,8 +22,8 @@ __global__ void __launch_bounds__(256) k_router(const float* __restrict__ logits
 
 template <int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) k_prepare(PrepArgs a) {
-  __shared__ prep::PrepSmem sm;
-  prep::prepare_body(a, sm);
+  extern __shared__ __align__(16) unsigned char prep_smem[];   // one PrepSmem (over the 48 KiB static limit)
+  prep::prepare_body(a, *reinterpret_cast<prep::PrepSmem*>(prep_smem));
 }
 
 // Copy the experts of the last prepare (misses -> their slots, or on bypass
@@ -155,8 +155,9 @@ cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s) {
   if (need > kPrepThreads) need = kPrepThreads;
   const int threads = (need + 31) / 32 * 32;
   if (a.do_route && a.T * a.k > prep::kMaxRoutedIds) return cudaErrorInvalidValue;
-  if (threads <= 256) k_prepare<256><<<1, threads, 0, s>>>(a);
-  else k_prepare<kPrepThreads><<<1, threads, 0, s>>>(a);
+  constexpr size_t smem = sizeof(prep::PrepSmem);
+  if (threads <= 256) k_prepare<256><<<1, threads, smem, s>>>(a);
+  else k_prepare<kPrepThreads><<<1, threads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -170,6 +171,11 @@ cudaError_t prepare_configure() {
   for (const void* k : kernels) {
     const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                                (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  for (const void* k : {(const void*)k_prepare<256>, (const void*)k_prepare<kPrepThreads>}) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(prep::PrepSmem));
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

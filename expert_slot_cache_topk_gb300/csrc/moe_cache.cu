@@ -81,6 +81,7 @@ struct moe_cache {
   int32_t* slot_map_d = nullptr;
   int32_t* slot_expert_d = nullptr;
   long long* slot_stamp_d = nullptr;
+  int32_t* slot_aux_d = nullptr;  // [L][N] per-slot policy state
   LayerState* state_d = nullptr;
   RecHdr* hdr_d = nullptr;
   int32_t* lists_d = nullptr;
@@ -224,6 +225,8 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
   a.slot_map = c->slot_map_d + (size_t)layer * c->E;
   a.slot_expert = c->slot_expert_d + (size_t)layer * c->N;
   a.slot_stamp = c->slot_stamp_d + (size_t)layer * c->N;
+  a.slot_aux = c->slot_aux_d + (size_t)layer * c->N;
+  a.policy = c->cfg.evict_policy;
   a.st = c->state_d + layer;
   a.hdr = c->hdr_d + layer;
   a.lists = c->lists_d + (size_t)layer * LST_COUNT * c->E;
@@ -523,7 +526,7 @@ void free_all(moe_cache* c) {
   if (c->ev_sync) cudaEventDestroy(c->ev_sync);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->fstack_d, c->counts_d, c->slot_map_d, c->slot_expert_d,
-                 c->slot_stamp_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
+                 c->slot_stamp_d, c->slot_aux_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
                  c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->tm_miss_d, c->xs_d[0], c->xs_d[1],
                  c->logits_stage_d, c->order_d, c->tiles_d, c->ntiles_d, c->gout_d, c->seq_d, c->ready_d};
   for (void* p : dev)
@@ -540,6 +543,7 @@ moe_status init_state(moe_cache* c) {
   if (N) {
     CK(c, cudaMemset(c->slot_expert_d, 0xFF, L * N * sizeof(int32_t)));
     CK(c, cudaMemset(c->slot_stamp_d, 0, L * N * sizeof(long long)));
+    CK(c, cudaMemset(c->slot_aux_d, 0, L * N * sizeof(int32_t)));
   }
   if (N) {
     std::vector<int32_t> fs(L * N);
@@ -609,6 +613,8 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   if (g.copy_mode < MOE_COPY_AUTO || g.copy_mode > MOE_COPY_FUSED)
     return fail(nullptr, MOE_EINVAL, "bad copy_mode");
   if (g.renormalize != 0 && g.renormalize != 1) return fail(nullptr, MOE_EINVAL, "renormalize must be 0 or 1");
+  if (g.evict_policy < MOE_EVICT_LRU || g.evict_policy > MOE_EVICT_SLRU)
+    return fail(nullptr, MOE_EINVAL, "evict_policy must be MOE_EVICT_LRU, _LFU, _FIFO or _SLRU");
   if (g.move_interval < 0) return fail(nullptr, MOE_EINVAL, "move_interval must be >= 0");
   if (g.move_interval > 0 && (!(g.move_decay > 0.f && g.move_decay <= 1.f) || !(g.move_threshold >= 0.f) ||
                               !(g.move_threshold < 3.0e38f) || g.move_count_tokens < 1))
@@ -690,6 +696,7 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   CKC(dmalloc((void**)&c->slot_map_d, L * E * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->slot_expert_d, L * N * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->slot_stamp_d, L * N * sizeof(long long)));
+  CKC(dmalloc((void**)&c->slot_aux_d, L * N * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->fstack_d, (L * N > 0 ? L * N : 1) * sizeof(int32_t)));
   if (g.move_interval > 0) CKC(dmalloc((void**)&c->counts_d, L * E * sizeof(float)));
   CKC(dmalloc((void**)&c->state_d, L * sizeof(LayerState)));

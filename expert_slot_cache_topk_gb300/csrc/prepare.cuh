@@ -1,6 +1,5 @@
-// Router top-k and per-layer slot bookkeeping as device functions, shared by
-// the standalone prepare kernel (k_route_prepare.cu) and the fused per-layer
-// kernel (k_mlp.cu), so both run the same code.
+// Router top-k and per-layer slot bookkeeping as device functions, used by
+// the prepare kernel (k_route_prepare.cu).
 //
 // Router: one warp per token; a logit is turned into an order-preserving
 // 32-bit key, and each of the k rounds takes two warp max-reductions (largest
@@ -161,12 +160,27 @@ struct PrepSmem {
   int fstack[MOE_MAX_EXPERTS];           // free-slot stack (the next miss takes fstack[nfree - 1])
   float counts[MOE_MAX_EXPERTS];         // use counts for run-time moves
   unsigned long long red[2][32];         // block reductions of the move decision
+  int aux[MOE_MAX_EXPERTS];              // per slot: LFU use count, or SLRU segment (1 = protected)
+  int hl[MOE_MAX_EXPERTS];               // this step's hits, ascending
+  unsigned char used[MOE_MAX_EXPERTS];   // slot hit in this step
   unsigned char newf[MOE_MAX_EXPERTS];   // expert copied in this step
   unsigned long long stats[ST_COUNT];    // the layer's counters, read at the start
   unsigned char cold[MOE_MAX_EXPERTS];
   int32_t ids[kMaxRoutedIds];
   int bad;
 };
+
+// Eviction order of an occupied slot (lower = evicted first): recency stamp
+// (LRU), insertion stamp (FIFO), (steps used, insertion stamp) (LFU),
+// (segment, recency stamp) with the probationary segment first (SLRU).
+// Stamps stay below 2^40 (each step advances the clock by at most 2E) and
+// LFU counts below 2^24.
+__device__ __forceinline__ unsigned long long evict_key(int pol, long long stamp, int aux) {
+  const unsigned long long st = (unsigned long long)stamp;
+  if (pol == MOE_EVICT_LFU) return ((unsigned long long)(unsigned)aux << 40) | st;
+  if (pol == MOE_EVICT_SLRU) return ((unsigned long long)(aux != 0) << 62) | st;
+  return st;
+}
 
 // Max (is_max) or min of one 64-bit value per thread over the CTA; every
 // thread must call it; the result is valid in thread 0.  buf holds 32 words.
@@ -221,6 +235,8 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
     S.sexp[q] = a.slot_expert[q];
     S.stamp[q] = a.slot_stamp[q];
     S.fstack[q] = a.free_stack[q];
+    S.aux[q] = a.slot_aux[q];
+    S.used[q] = 0;
   }
   if (tid - l0 >= 0 && tid - l0 < ST_COUNT) S.stats[tid - l0] = a.st->stats[tid - l0];
   if (tid == 0) S.bad = 0;
@@ -277,18 +293,68 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
     const int r_h = rank[3], r_m = rank[4];
     nh = tot[3];
     nm = tot[4];
+    const int pol = a.policy;
     if (hit) {
-      S.stamp[S.map[e]] = (long long)(clk + (unsigned long long)r_h);   // touch: newest stamps
+      const int hs = S.map[e];
+      S.used[hs] = 1;
+      if (pol == MOE_EVICT_LRU) S.stamp[hs] = (long long)(clk + (unsigned long long)r_h);   // touch: newest
+      else if (pol == MOE_EVICT_LFU) S.aux[hs] += 1;                                        // one more step used
       a.lists[LST_HITS * E + r_h] = e;
+      S.hl[r_h] = e;
     }
     nvict = nm > nfree ? nm - nfree : 0;
     __syncthreads();
-    if (nvict > 0 && tid < N && S.sexp[tid] >= 0) {
-      // rank of this slot by recency among occupied slots (stamps are unique);
-      // hits were just stamped newest, so the nvict oldest are not in this step
-      const long long my = S.stamp[tid];
+    if (pol == MOE_EVICT_SLRU && tid < 32 && nh > 0) {
+      // warp 0 takes the hits in ascending id order: a probationary expert
+      // moves to the protected MRU end, and if that overflows the protected
+      // segment (floor(4N/5)), the protected LRU expert moves to the
+      // probationary MRU end; a protected expert moves to its MRU end
+      const int cap = (4 * N) / 5;
+      int np = 0;
+      for (int s2 = tid; s2 < N; s2 += 32) np += (S.sexp[s2] >= 0 && S.aux[s2] == 1);
+      int nprot = __reduce_add_sync(0xffffffffu, np);
+      unsigned long long c2 = clk;
+      for (int r = 0; r < nh; ++r) {
+        const int hs = S.map[S.hl[r]];
+        const bool promote = S.aux[hs] == 0;
+        __syncwarp();
+        if (tid == 0) {
+          S.stamp[hs] = (long long)c2;
+          S.aux[hs] = 1;
+        }
+        ++c2;
+        __syncwarp();
+        if (promote && ++nprot > cap) {
+          unsigned long long lo = ~0ull;   // (stamp << 10 | slot) of the protected LRU expert
+          for (int s2 = tid; s2 < N; s2 += 32)
+            if (S.sexp[s2] >= 0 && S.aux[s2] == 1) {
+              const unsigned long long v = ((unsigned long long)S.stamp[s2] << 10) | (unsigned)s2;
+              lo = v < lo ? v : lo;
+            }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long u = __shfl_xor_sync(0xffffffffu, lo, o);
+            lo = u < lo ? u : lo;
+          }
+          if (tid == 0) {
+            const int ls = (int)(lo & 1023u);
+            S.aux[ls] = 0;
+            S.stamp[ls] = (long long)c2;
+          }
+          ++c2;
+          --nprot;
+          __syncwarp();
+        }
+      }
+    }
+    __syncthreads();
+    if (nvict > 0 && tid < N && S.sexp[tid] >= 0 && !S.used[tid]) {
+      // rank of this slot among the occupied slots not used in this step, by
+      // the policy's key (unique): the nvict lowest are the victims
+      const unsigned long long my = evict_key(pol, S.stamp[tid], S.aux[tid]);
       int r = 0;
-      for (int s2 = 0; s2 < N; ++s2) r += (S.sexp[s2] >= 0 && S.stamp[s2] < my);
+      for (int s2 = 0; s2 < N; ++s2)
+        r += (S.sexp[s2] >= 0 && !S.used[s2] && evict_key(pol, S.stamp[s2], S.aux[s2]) < my);
       if (r < nvict) S.victim[r] = tid;
     }
     __syncthreads();
@@ -297,7 +363,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
       if (r_m < nfree) {
         slot = S.fstack[nfree - 1 - r_m];      // free-slot stack, popped from the end
       } else {
-        slot = S.victim[r_m - nfree];          // i-th least recently used slot
+        slot = S.victim[r_m - nfree];          // i-th victim of the policy
         ev = S.sexp[slot];
       }
       a.lists[LST_MISS_E * E + r_m] = e;
@@ -310,7 +376,8 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
       S.newf[e] = 1;
       S.map[e] = slot;
       S.sexp[slot] = e;
-      S.stamp[slot] = (long long)(clk + (unsigned long long)(nh + r_m));
+      S.stamp[slot] = (long long)(clk + (unsigned long long)(2 * nh + r_m));   // insertion: newest
+      S.aux[slot] = a.policy == MOE_EVICT_LFU ? 1 : 0;                        // used in one step; probationary
     }
   }
   __syncthreads();
@@ -319,6 +386,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
     if (tid < N) {
       a.slot_expert[tid] = S.sexp[tid];
       a.slot_stamp[tid] = S.stamp[tid];
+      a.slot_aux[tid] = S.aux[tid];
     }
   }
 
@@ -334,7 +402,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
       sv[ST_BYPASS] += 1;
       sv[ST_B_BYPASS] += (unsigned long long)D * a.expert_bytes;
     } else {
-      st->clock = clk + (unsigned long long)(nh + nm);
+      st->clock = clk + (unsigned long long)(2 * nh + nm);
       st->nfree = nfree - (nm < nfree ? nm : nfree);
       sv[ST_HITS] += (unsigned long long)nh;
       sv[ST_MISSES] += (unsigned long long)nm;

@@ -100,6 +100,21 @@ typedef enum { MOE_COPY_AUTO = 0, MOE_COPY_MEMCPY = 1, MOE_COPY_UVA = 2, MOE_COP
  * rounding. */
 typedef enum { MOE_MLP_AUTO = 0, MOE_MLP_PLAIN = 1 } moe_mlp_kernel;
 
+/* Which resident expert a miss evicts when no slot is free ([vLLM #37190],
+ * the review thread that added a cache-policy option).  Under every policy an
+ * expert used in the current step is never evicted, hits are booked before
+ * misses and both go in ascending expert id.
+ *   LRU   least recently used (a hit refreshes).
+ *   LFU   fewest steps used since it was inserted; ties to the earliest inserted.
+ *   FIFO  earliest inserted (a hit does not refresh).
+ *   SLRU  two segments: misses enter the probationary one; a hit there moves
+ *         the expert to the protected one's most recent end, which holds at
+ *         most floor(4N/5) experts (overflow moves the protected least recent
+ *         one to the probationary most recent end); a hit in the protected one
+ *         refreshes it.  The victim is the probationary least recent expert,
+ *         else the protected least recent one. */
+typedef enum { MOE_EVICT_LRU = 0, MOE_EVICT_LFU = 1, MOE_EVICT_FIFO = 2, MOE_EVICT_SLRU = 3 } moe_evict_policy;
+
 typedef enum {
   MOE_OK = 0,
   MOE_EINVAL = -1,    /* bad argument, nothing done */
@@ -157,6 +172,7 @@ typedef struct {
   float move_decay;      /* (0, 1] */
   float move_threshold;  /* >= 0 */
   int move_count_tokens; /* >= 1 */
+  int evict_policy;      /* moe_evict_policy */
 } moe_cache_config;
 
 /* Cumulative per-layer counters (moe_cache_stats with layer = -1 sums layers).
