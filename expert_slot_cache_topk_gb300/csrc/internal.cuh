@@ -38,11 +38,15 @@ enum { LST_HITS = 0, LST_MISS_E, LST_MISS_SLOT, LST_MISS_EV, LST_COLD, LST_NONCO
 // Device error flag values (sticky until reset)
 enum { DEVERR_NONE = 0, DEVERR_BAD_ID = 1, DEVERR_BARRIER = 2, DEVERR_RING = 3 };
 
-// Grid-wide barrier state of the fused MLP kernel (count returns to 0 after
-// every barrier; gen counts completed barriers).
+// Grid-wide barrier state.  The cooperative MLP kernel uses count / gen
+// (count returns to 0 after every barrier; gen counts completed barriers);
+// the staged kernel uses arrivals, which only grows: every barrier adds one
+// per CTA, so a CTA whose arrival returned a waits until arrivals reaches the
+// next multiple of the grid size.
 struct GridBar {
   unsigned count;
   unsigned gen;
+  unsigned long long arrivals;
 };
 
 struct PrepArgs {

@@ -55,7 +55,6 @@ constexpr int kMaxStages = 12;
 constexpr int kMaxRows = 64;                        // output rows per CTA whose residual is kept in shared memory
 constexpr int kParts = 4;                           // parts per output row in the down phase
 constexpr int kRowsPerPass = kConsumers / kParts;   // output rows the consumer warps take at once
-constexpr int kBatch = 8;                           // chunks per lane in flight on the plain-load paths
 constexpr unsigned long long kWaitNs = 500000000ull;  // 0.5 s
 constexpr size_t kSmemLimit = 227 * 1024;
 
@@ -80,7 +79,6 @@ struct RingShared {
   float gu[kMaxStages][kConsumers / 2][2]; // up, half-size items: gate / up sums of each pair
   int cnt[kMaxStages][kConsumers / 2];     // up, half-size items: rows of the pair finished
   int stop;                                // set when a wait ran out: skip the rest
-  unsigned long long hbar;                 // the bulk copy of h has landed
 };
 
 struct RingCfg {
@@ -89,7 +87,6 @@ struct RingCfg {
   unsigned stage_bytes;   // bytes per stage (multiple of 128)
   int down_rows;          // output rows per down item (<= kConsumers)
   int down_group;         // CTA row ranges start at multiples of this (8 for INT4 scale rows)
-  unsigned h_off;         // byte offset of the h copy (k * I f32) after the ring stages
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -144,37 +141,40 @@ __device__ __forceinline__ bool in_host(const MlpArgs& a, unsigned long long p) 
 }
 
 // Grid barrier among the consumer warps of every CTA (the producer warps do
-// not take part).  The CTA's writes are ordered before the arrival by the
-// CTA barrier plus one thread's fence (fences are cumulative); that thread
-// polls the generation word with acquire loads.  Bounded: gives up after
-// ~1 s and flags DEVERR_BARRIER.
+// not take part).  The CTA's writes are ordered before its arrival by the CTA
+// barrier plus one thread's release add (release is cumulative); that thread
+// polls the arrival count with acquire loads until every CTA of this launch
+// has arrived -- one atomic per CTA, no reset.  Bounded: gives up after ~1 s
+// and flags DEVERR_BARRIER.
 __device__ __forceinline__ void consumer_grid_barrier(GridBar* bar, int* err, int ctid) {
-  // h written here is read by another CTA's bulk copy (async proxy)
-  asm volatile("fence.proxy.async.global;" ::: "memory");
   consumer_sync();
   if (ctid == 0) {
-    const unsigned gen = *reinterpret_cast<volatile unsigned*>(&bar->gen);
-    __threadfence();
-    const unsigned arrived = atomicAdd(&bar->count, 1u);
-    if (arrived == gridDim.x - 1) {
-      atomicExch(&bar->count, 0u);
-      __threadfence();
-      atomicAdd(&bar->gen, 1u);
-    } else {
-      const unsigned long long t0 = global_ns();
-      for (unsigned it = 0;; ++it) {
-        unsigned g;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(&bar->gen) : "memory");
-        if (g != gen) break;
-        if ((it & 255u) == 255u && global_ns() - t0 > 1000000000ull) {
-          atomicExch(err, DEVERR_BARRIER);
-          break;
-        }
+    const unsigned long long G = gridDim.x;
+    unsigned long long old;
+    asm volatile("atom.release.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(&bar->arrivals) : "memory");
+    const unsigned long long target = (old / G + 1ull) * G;
+    const unsigned long long t0 = global_ns();
+    for (unsigned it = 0;; ++it) {
+      unsigned long long v;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(&bar->arrivals) : "memory");
+      if (v >= target) break;
+      if ((it & 255u) == 255u && global_ns() - t0 > 1000000000ull) {
+        atomicExch(err, DEVERR_BARRIER);
+        break;
       }
     }
-    __threadfence();
   }
   consumer_sync();
+}
+
+// 16 bytes of data written by other CTAs in this launch (after a grid
+// barrier): read at L2, never from this SM's L1
+__device__ __forceinline__ float4 ld_l2_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
 }
 
 // x[0, n] as f32, and y[0, n] = v (bf16 unless F is f32)
@@ -686,26 +686,8 @@ __device__ __forceinline__ void consume(const MlpArgs& a, const RingCfg& rc, Rin
     const int Qp = (Q + kParts - 1) / kParts;
     const int pt = cw % kParts;
     const int q_end = min(Q, (pt + 1) * Qp);
-    // h (k * I f32) -> shared memory in one bulk copy, then this warp's part
-    // of it -> registers
-    const float* hs = reinterpret_cast<const float*>(ring + rc.h_off);
-    const unsigned hbytes = (unsigned)(a.k * a.I * 4);
-    if (ctid == 0) {
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      mbar_arrive_tx(smem_u32(&S.hbar), hbytes);
-      for (unsigned o = 0; o < hbytes; o += 16384u)
-        bulk_copy(smem_u32(ring + rc.h_off + o), reinterpret_cast<const uint8_t*>(a.h) + o,
-                  hbytes - o < 16384u ? hbytes - o : 16384u, smem_u32(&S.hbar));
-    }
-    // every consumer waits (bounded), so the copy has landed before the CTA can exit
-    const bool h_ok = mbar_wait(smem_u32(&S.hbar), 0u);
-    if (!h_ok && !dead) {
-      dead = true;
-      if (lane == 0) {
-        atomicExch(err, DEVERR_RING);
-        *stop = 1;
-      }
-    }
+    // this warp's part of h (k * I f32, written by every CTA) -> registers,
+    // straight from L2
     float hr[HM][EL];
     int qj[HM];
 #pragma unroll
@@ -717,10 +699,10 @@ __device__ __forceinline__ void consume(const MlpArgs& a, const RingCfg& rc, Rin
       if (q < q_end) {
         const int j = q / C2;
         qj[m] = (j << 16) | (q - j * C2);
-        const float4* src = reinterpret_cast<const float4*>(hs + (size_t)q * EL);
+        const float* src = a.h + (size_t)q * EL;
 #pragma unroll
         for (int e = 0; e < EL / 4; ++e) {
-          const float4 v = src[e];
+          const float4 v = ld_l2_f4(src + 4 * e);
           hr[m][4 * e] = v.x;
           hr[m][4 * e + 1] = v.y;
           hr[m][4 * e + 2] = v.z;
@@ -780,7 +762,6 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_mlp_ring(MlpArgs a, RingCfg
     }
     S.stop = 0;
     for (int q = 0; q < kMaxStages * (kConsumers / 2); ++q) (&S.cnt[0][0])[q] = 0;
-    mbar_init(smem_u32(&S.hbar), 1u);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -831,17 +812,15 @@ bool ring_geometry(int F, int H, int I, int k, RingCfg* rc, size_t* dyn_smem) {
   sb = (sb + 127) / 128 * 128;
   // static shared memory (the ring starts 1024-byte aligned after it) + reserve
   const size_t fixed = (sizeof(RingShared) + 1023) / 1024 * 1024 + 1024;
-  const size_t hbytes = ((size_t)k * I * 4 + 127) / 128 * 128;   // f32 h after the barrier
-  if (fixed + hbytes + 2 * sb > kSmemLimit) return false;
-  size_t ns = (kSmemLimit - fixed - hbytes) / sb;
+  if (fixed + 2 * sb > kSmemLimit) return false;
+  size_t ns = (kSmemLimit - fixed) / sb;
   if (ns > (size_t)kMaxStages) ns = kMaxStages;
   rc->up_pairs = P;
   rc->nstages = (int)ns;
   rc->stage_bytes = (unsigned)sb;
   rc->down_rows = down_rows;
   rc->down_group = down_group;
-  rc->h_off = (unsigned)(ns * sb);
-  *dyn_smem = ns * sb + hbytes;
+  *dyn_smem = ns * sb;
   return true;
 }
 
