@@ -54,6 +54,7 @@ constexpr int kRingThreads = 32 * (1 + kConsumers);
 constexpr int kMaxStages = 12;
 constexpr int kMaxRows = 64;                        // output rows per CTA whose residual is kept in shared memory
 constexpr int kParts = 4;                           // parts per output row in the down phase
+static_assert(kParts == 4, "down_store sums four parts");
 constexpr int kRowsPerPass = kConsumers / kParts;   // output rows the consumer warps take at once
 constexpr unsigned long long kWaitNs = 500000000ull;  // 0.5 s
 constexpr size_t kSmemLimit = 227 * 1024;
@@ -75,7 +76,7 @@ struct RingShared {
   unsigned long long base[MOE_MAX_TOPK];   // block pointer of each assignment
   float wt[MOE_MAX_TOPK];                  // router weight of each assignment
   float xres[kMaxRows];                    // residual x of this CTA's output rows
-  float part[2][kParts * kConsumers];      // down: the part sums of each row, by item parity
+  float part[kMaxRows * kParts];           // down: the part sums of each of the CTA's rows
   float gu[kMaxStages][kConsumers / 2][2]; // up, half-size items: gate / up sums of each pair
   int cnt[kMaxStages][kConsumers / 2];     // up, half-size items: rows of the pair finished
   int stop;                                // set when a wait ran out: skip the rest
@@ -131,6 +132,25 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, unsigne
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(bar)
       : "memory");
+}
+// the same, with an L2 eviction-priority policy for the source lines
+__device__ __forceinline__ void bulk_copy_hint(uint32_t dst, const void* src, unsigned bytes, uint32_t bar,
+                                               unsigned long long policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+// weight rows read once per launch go first when L2 needs room
+__device__ __forceinline__ unsigned long long evict_first_policy() {
+  unsigned long long p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// bytes (multiple of 16) from global src (16-byte aligned) into L2, no wait
+__device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(src)), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
@@ -531,8 +551,17 @@ __device__ __forceinline__ void produce(const MlpArgs& a, const RingCfg& rc, Rin
   const unsigned plain_mask = __ballot_sync(kFull, plain);
   const unsigned k_mask = a.k >= 32 ? kFull : ((1u << a.k) - 1u);
   const int n_ring = __popc(k_mask & ~plain_mask);
+  const unsigned long long pol_first = evict_first_policy();
   int i = 0;
   for (; i < w.n_items; ++i) {
+    if (i == w.n_up && w.n_items - w.n_up > NS && lane < a.k && !plain) {
+      // the W2 rows of the down items that wait for a free stage: into L2 now,
+      // while the grid meets, so that their copies after the barrier are short
+      const int nr0 = w.n0 + NS * rc.down_rows;
+      const uint8_t* blk = reinterpret_cast<const uint8_t*>(myb);
+      prefetch_l2(blk + a.off_w2 + (size_t)nr0 * rb2, (unsigned)((size_t)(w.n1 - nr0) * rb2));
+      if (srb2 != 0) prefetch_l2(blk + a.off_s2 + (size_t)nr0 * srb2, (unsigned)((size_t)(w.n1 - nr0) * srb2));
+    }
     const int s = i % NS;
     const uint32_t full = smem_u32(&S.full[s]);
     uint8_t* st = ring + (size_t)s * rc.stage_bytes;
@@ -559,12 +588,12 @@ __device__ __forceinline__ void produce(const MlpArgs& a, const RingCfg& rc, Rin
         if (lane == 0) mbar_arrive_tx(full, 2u * (wb + sb));
         __syncwarp();
         const uint8_t* w13 = reinterpret_cast<const uint8_t*>(blk);
-        if (lane == 0) bulk_copy(smem_u32(st), w13 + (size_t)p0 * rb1, wb, full);
-        if (lane == 1) bulk_copy(smem_u32(st + wb), w13 + (size_t)(a.I + p0) * rb1, wb, full);
+        if (lane == 0) bulk_copy_hint(smem_u32(st), w13 + (size_t)p0 * rb1, wb, full, pol_first);
+        if (lane == 1) bulk_copy_hint(smem_u32(st + wb), w13 + (size_t)(a.I + p0) * rb1, wb, full, pol_first);
         if (sb != 0u) {
           const uint8_t* s13 = w13 + a.off_s13;
-          if (lane == 2) bulk_copy(smem_u32(st + 2 * wb), s13 + (size_t)p0 * srb1, sb, full);
-          if (lane == 3) bulk_copy(smem_u32(st + 2 * wb + sb), s13 + (size_t)(a.I + p0) * srb1, sb, full);
+          if (lane == 2) bulk_copy_hint(smem_u32(st + 2 * wb), s13 + (size_t)p0 * srb1, sb, full, pol_first);
+          if (lane == 3) bulk_copy_hint(smem_u32(st + 2 * wb + sb), s13 + (size_t)(a.I + p0) * srb1, sb, full, pol_first);
         }
       } else if (lane == 0) {
         mbar_arrive(full);
@@ -595,6 +624,20 @@ __device__ __forceinline__ void produce(const MlpArgs& a, const RingCfg& rc, Rin
       if (!mbar_wait(smem_u32(&S.full[q % NS]), (unsigned)(q / NS) & 1u)) atomicExch(err, DEVERR_RING);
   }
   __syncwarp();
+}
+
+// y for output rows n0 + r, r < nr, from their part sums (part + kParts r),
+// one consumer thread per row, parts summed in a fixed order
+template <int F>
+__device__ __forceinline__ void down_store(const MlpArgs& a, const RingShared& S, const float* part, int n0, int nr,
+                                           int cta_n0, int ctid) {
+  for (int r = ctid; r < nr; r += 32 * kConsumers) {
+    const float* pr = part + kParts * r;
+    const int n = n0 + r;
+    float v = (pr[0] + pr[1]) + (pr[2] + pr[3]);
+    if (a.residual) v += n - cta_n0 < kMaxRows ? S.xres[n - cta_n0] : x_at<F>(a, n);
+    store_out<F>(a, n, v);
+  }
 }
 
 // ------------------------------------------------------- consumer driver
@@ -723,21 +766,23 @@ __device__ __forceinline__ void consume(const MlpArgs& a, const RingCfg& rc, Rin
           }
         }
       }
-      float* part = S.part[i & 1];
       const RingDesc d = S.desc[s];
+      // part sums go to the row's place in S.part; a CTA with more rows than
+      // that holds reuses it from the start, one item at a time
+      const bool all_rows = w.n1 - w.n0 <= kMaxRows;
+      float* part = S.part + (all_rows ? kParts * (d.p0 - w.n0) : 0);
       if (!dead) down_rows<F>(a, S, d, ring + (size_t)s * rc.stage_bytes, hr, qj, part, cw, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
-      consumer_sync();   // every part of every row of the item is in part[]
-      if (!dead && pt == 0 && lane == 0) {
-        for (int r = cw / kParts; r < d.n; r += kRowsPerPass) {
-          const float* pr = part + kParts * r;
-          const int n = d.p0 + r;
-          float v = (pr[0] + pr[1]) + (pr[2] + pr[3]);
-          if (a.residual) v += n - w.n0 < kMaxRows ? S.xres[n - w.n0] : x_at<F>(a, n);
-          store_out<F>(a, n, v);
-        }
+      if (!all_rows) {
+        consumer_sync();   // every part of every row of the item is in part[]
+        if (!dead) down_store<F>(a, S, part, d.p0, d.n, w.n0, ctid);
+        consumer_sync();   // part[] is free for the next item
       }
+    }
+    if (w.n1 - w.n0 <= kMaxRows) {
+      consumer_sync();     // every part of every row of the CTA is in S.part
+      if (!dead) down_store<F>(a, S, S.part, w.n0, w.n1 - w.n0, w.n0, ctid);
     }
   }
 }
