@@ -390,14 +390,20 @@ def run_ours(args, w):
     # MEMCPY mode takes a host decision per layer step, so it cannot be captured
     use_graph = not args.no_graph and info["copy_mode_name"] != "memcpy"
 
-    def prime(timing: bool):
-        """Empty the pools, run the warm-up steps, then capture (or not) the timed
-        steps; returns (graph or None, kernel launches of the timed steps)."""
+    def warm():
         c.reset()
         with torch.cuda.stream(stream):
             for s in range(args.warmup):
                 step(s, stream)
         stream.synchronize()
+
+    def prime(timing: bool):
+        """Empty the pools, run the warm-up steps, then capture (or not) the timed
+        steps; returns (graph or None, kernel launches of the timed steps).  The
+        uninstrumented graph is replayed once untimed (its first launch uploads
+        it to the device), then the pools are emptied and warmed up again, so
+        that the timed replay starts from the state the capture saw."""
+        warm()
         c.set_timing(timing, capacity=args.steps * w.layers + 64)
         l0 = c.info()["kernel_launches"]
         g = None
@@ -408,6 +414,13 @@ def run_ours(args, w):
                     for s in range(args.warmup, S):
                         step(s, stream)
             stream.synchronize()
+            n = c.info()["kernel_launches"] - l0
+            if not timing:
+                with torch.cuda.stream(stream):
+                    g.replay()
+                stream.synchronize()
+                warm()
+            return g, n
         return g, c.info()["kernel_launches"] - l0
 
     def timed(g, sampler_ms):

@@ -155,6 +155,8 @@ size_t mlp_up_smem_bytes(int H);
 // shared memory by bulk copies; cudaErrorNotSupported = use launch_mlp_fused.
 cudaError_t mlp_ring_configure(int wdtype, int H, int I, int k);  // call outside capture
 cudaError_t launch_mlp_ring(int wdtype, const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s);
+// floats the staged kernel's h scratch needs (it keeps several copies of h)
+size_t mlp_ring_h_floats(int k, int I);
 
 // ---- launchers (k_moe_gemm.cu): grouped expert MLP on the tensor cores for
 // steps with several tokens (group by expert, tcgen05 up and down GEMMs,

@@ -53,6 +53,7 @@ constexpr int kConsumers = 8;                       // consumer warps
 constexpr int kRingThreads = 32 * (1 + kConsumers);
 constexpr int kMaxStages = 12;
 constexpr int kMaxRows = 64;                        // output rows per CTA whose residual is kept in shared memory
+constexpr int kHRep = 8;                            // copies of h in global memory (read spread over L2)
 constexpr int kParts = 4;                           // parts per output row in the down phase
 static_assert(kParts == 4, "down_store sums four parts");
 constexpr int kRowsPerPass = kConsumers / kParts;   // output rows the consumer warps take at once
@@ -359,7 +360,9 @@ __device__ __forceinline__ void up_item(const MlpArgs& a, RingShared& S, const R
       uint4* const cpys[2] = {copy ? cpyp(cw) : nullptr, copy ? cpyp(P + cw) : nullptr};
       rows_dot<F, 2>(rows, srows, cpys, ring, copy, C, xr, lane, v);
     }
-    if (lane == 0) a.h[(size_t)d.asg * a.I + d.p0 + cw] = swiglu_h(S, base, d.asg, v[0], v[1]);
+    // every lane holds the sums: lanes 0..kHRep-1 write one copy of h each
+    if (lane < kHRep)
+      a.h[(size_t)lane * a.k * a.I + (size_t)d.asg * a.I + d.p0 + cw] = swiglu_h(S, base, d.asg, v[0], v[1]);
   } else {
     float v[1] = {0.f};
     if (d.src != SRC_NONE) {
@@ -376,7 +379,8 @@ __device__ __forceinline__ void up_item(const MlpArgs& a, RingShared& S, const R
         __threadfence_block();
         const float g = S.gu[s][pr][0], u = S.gu[s][pr][1];
         S.cnt[s][pr] = 0;
-        a.h[(size_t)d.asg * a.I + d.p0 + pr] = swiglu_h(S, base, d.asg, g, u);
+        const float hv = swiglu_h(S, base, d.asg, g, u);
+        for (int r = 0; r < kHRep; ++r) a.h[(size_t)r * a.k * a.I + (size_t)d.asg * a.I + d.p0 + pr] = hv;
       }
     }
   }
@@ -742,7 +746,9 @@ __device__ __forceinline__ void consume(const MlpArgs& a, const RingCfg& rc, Rin
       if (q < q_end) {
         const int j = q / C2;
         qj[m] = (j << 16) | (q - j * C2);
-        const float* src = a.h + (size_t)q * EL;
+        // every CTA reads all of h: copy blockIdx % kHRep, so that the reads
+        // of the grid spread over kHRep times as many L2 lines
+        const float* src = a.h + (size_t)(blockIdx.x % kHRep) * a.k * a.I + (size_t)q * EL;
 #pragma unroll
         for (int e = 0; e < EL / 4; ++e) {
           const float4 v = ld_l2_f4(src + 4 * e);
@@ -791,6 +797,10 @@ template <int F>
 __global__ void __launch_bounds__(kRingThreads, 1) k_mlp_ring(MlpArgs a, RingCfg rc, GridBar* bar, int* err) {
   extern __shared__ __align__(1024) uint8_t ring[];
   __shared__ RingShared S;
+  // the next kernel of the stream (a prepare launched as a programmatic
+  // dependent) may be scheduled now: it waits for this grid to complete
+  // before it touches memory, and its CTA fits beside this one
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < a.k) {
     S.base[threadIdx.x] = a.asg_ptr[threadIdx.x];
@@ -927,6 +937,8 @@ cudaError_t ring_impl(const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s) 
 }
 
 }  // namespace
+
+size_t mlp_ring_h_floats(int k, int I) { return (size_t)kHRep * k * I; }
 
 cudaError_t mlp_ring_configure(int wdtype, int H, int I, int k) {
   switch (wdtype) {

@@ -22,8 +22,13 @@ __global__ void __launch_bounds__(256) k_router(const float* __restrict__ logits
 
 template <int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) k_prepare(PrepArgs a) {
-  extern __shared__ __align__(16) unsigned char prep_smem[];   // one PrepSmem (over the 48 KiB static limit)
-  prep::prepare_body(a, *reinterpret_cast<prep::PrepSmem*>(prep_smem));
+  extern __shared__ __align__(16) unsigned char prep_smem[];
+  // Launched early behind the previous kernel of the stream (programmatic
+  // dependent launch): wait for it to complete before any global access.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  prep::PrepSmem S;
+  prep::prep_smem_layout(a.E, a.N, a.do_route ? a.T * a.k : 0, prep_smem, &S);
+  prep::prepare_body(a, S);
 }
 
 // Copy the experts of the last prepare (misses -> their slots, or on bypass
@@ -155,10 +160,21 @@ cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s) {
   if (need > kPrepThreads) need = kPrepThreads;
   const int threads = (need + 31) / 32 * 32;
   if (a.do_route && a.T * a.k > prep::kMaxRoutedIds) return cudaErrorInvalidValue;
-  constexpr size_t smem = sizeof(prep::PrepSmem);
-  if (threads <= 256) k_prepare<256><<<1, threads, smem, s>>>(a);
-  else k_prepare<kPrepThreads><<<1, threads, smem, s>>>(a);
-  return cudaGetLastError();
+  const size_t smem = prep::prep_smem_layout(a.E, a.N, a.do_route ? a.T * a.k : 0, nullptr, nullptr);
+  // programmatic dependent launch: the CTA may be scheduled while the previous
+  // kernel (which triggers early) still runs, and waits for it on the device
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (threads <= 256) return cudaLaunchKernelEx(&cfg, k_prepare<256>, a);
+  return cudaLaunchKernelEx(&cfg, k_prepare<kPrepThreads>, a);
 }
 
 // Every kernel of a layer step prefers the largest shared-memory carve-out,
@@ -174,8 +190,9 @@ cudaError_t prepare_configure() {
     if (e != cudaSuccess) return e;
   }
   for (const void* k : {(const void*)k_prepare<256>, (const void*)k_prepare<kPrepThreads>}) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(prep::PrepSmem));
+    const cudaError_t e = cudaFuncSetAttribute(
+        k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)prep::prep_smem_layout(MOE_MAX_EXPERTS, MOE_MAX_EXPERTS, prep::kMaxRoutedIds, nullptr, nullptr));
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -707,7 +707,8 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   CKC(dmalloc((void**)&c->src_d, TK * sizeof(unsigned long long)));
   CKC(dmalloc((void**)&c->ids_d, TK * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->w_d, TK * sizeof(float)));
-  CKC(dmalloc((void**)&c->h_d, TK * c->I * sizeof(float)));
+  const size_t h_floats = TK * c->I > mlp_ring_h_floats(c->K, c->I) ? TK * c->I : mlp_ring_h_floats(c->K, c->I);
+  CKC(dmalloc((void**)&c->h_d, h_floats * sizeof(float)));
   CKC(dmalloc((void**)&c->err_d, sizeof(int)));
   CKC(dmalloc((void**)&c->bar_d, sizeof(GridBar)));
   CKC(dmalloc((void**)&c->seq_d, sizeof(unsigned)));

@@ -149,26 +149,81 @@ __device__ __forceinline__ void block_scan_multi(const int (&flag)[NF], int (&ra
   }
 }
 
+// Shared state of one prepare CTA, carved out of dynamic shared memory at
+// sizes for this layer (E experts, N slots, n_ids routed ids), so that a small
+// layer needs a few KiB and its prepare CTA fits on an SM beside a resident
+// expert-MLP CTA.
 struct PrepSmem {
-  int c[5][33];
-  int map[MOE_MAX_EXPERTS];        // expert -> slot (-1 absent)
-  int rank[MOE_MAX_EXPERTS];       // rank among the step's non-cold experts
-  int sexp[MOE_MAX_EXPERTS];       // slot -> expert (-1 free)
-  long long stamp[MOE_MAX_EXPERTS];
-  int victim[MOE_MAX_EXPERTS];
-  int nsel[MOE_MAX_EXPERTS];             // assignments of each expert in this step
-  int fstack[MOE_MAX_EXPERTS];           // free-slot stack (the next miss takes fstack[nfree - 1])
-  float counts[MOE_MAX_EXPERTS];         // use counts for run-time moves
-  unsigned long long red[2][32];         // block reductions of the move decision
-  int aux[MOE_MAX_EXPERTS];              // per slot: LFU use count, or SLRU segment (1 = protected)
-  int hl[MOE_MAX_EXPERTS];               // this step's hits, ascending
-  unsigned char used[MOE_MAX_EXPERTS];   // slot hit in this step
-  unsigned char newf[MOE_MAX_EXPERTS];   // expert copied in this step
-  unsigned long long stats[ST_COUNT];    // the layer's counters, read at the start
-  unsigned char cold[MOE_MAX_EXPERTS];
-  int32_t ids[kMaxRoutedIds];
-  int bad;
+  long long* stamp;                  // [N]
+  unsigned long long (*red)[32];     // [2][32] block reductions of the move decision
+  unsigned long long* stats;         // [ST_COUNT] the layer's counters, read at the start
+  int (*c)[33];                      // [5][33] block scan
+  int* map;                          // [E] expert -> slot (-1 absent)
+  int* rank;                         // [E] rank among the step's non-cold experts
+  int* nsel;                         // [E] assignments of each expert in this step
+  float* counts;                     // [E] use counts for run-time moves
+  int* sexp;                         // [N] slot -> expert (-1 free)
+  int* victim;                       // [N]
+  int* fstack;                       // [N] free-slot stack (the next miss takes fstack[nfree - 1])
+  int* aux;                          // [N] LFU use count, or SLRU segment (1 = protected)
+  int* hl;                           // [N] this step's hits, ascending
+  int32_t* ids;                      // [n_ids] routed ids (fused router)
+  int* bad;                          // an id out of range
+  unsigned char* used;               // [N] slot hit in this step
+  unsigned char* newf;               // [E] expert copied in this step
+  unsigned char* cold;               // [E]
 };
+
+// Byte size of the state for (E, N, n_ids); with base != null also points the
+// fields of S into base (16-byte aligned).
+__host__ __device__ inline size_t prep_smem_layout(int E, int N, int n_ids, unsigned char* base, PrepSmem* S) {
+  const size_t e = E > 0 ? (size_t)E : 1, n = N > 0 ? (size_t)N : 1, t = n_ids > 0 ? (size_t)n_ids : 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = (o + bytes + 15) / 16 * 16;
+    return base ? base + at : nullptr;
+  };
+  unsigned char* p_stamp = take(n * 8);
+  unsigned char* p_red = take(2 * 32 * 8);
+  unsigned char* p_stats = take(ST_COUNT * 8);
+  unsigned char* p_c = take(5 * 33 * 4);
+  unsigned char* p_map = take(e * 4);
+  unsigned char* p_rank = take(e * 4);
+  unsigned char* p_nsel = take(e * 4);
+  unsigned char* p_counts = take(e * 4);
+  unsigned char* p_sexp = take(n * 4);
+  unsigned char* p_victim = take(n * 4);
+  unsigned char* p_fstack = take(n * 4);
+  unsigned char* p_aux = take(n * 4);
+  unsigned char* p_hl = take(n * 4);
+  unsigned char* p_ids = take(t * 4);
+  unsigned char* p_bad = take(4);
+  unsigned char* p_used = take(n);
+  unsigned char* p_newf = take(e);
+  unsigned char* p_cold = take(e);
+  if (base && S) {
+    S->stamp = reinterpret_cast<long long*>(p_stamp);
+    S->red = reinterpret_cast<unsigned long long(*)[32]>(p_red);
+    S->stats = reinterpret_cast<unsigned long long*>(p_stats);
+    S->c = reinterpret_cast<int(*)[33]>(p_c);
+    S->map = reinterpret_cast<int*>(p_map);
+    S->rank = reinterpret_cast<int*>(p_rank);
+    S->nsel = reinterpret_cast<int*>(p_nsel);
+    S->counts = reinterpret_cast<float*>(p_counts);
+    S->sexp = reinterpret_cast<int*>(p_sexp);
+    S->victim = reinterpret_cast<int*>(p_victim);
+    S->fstack = reinterpret_cast<int*>(p_fstack);
+    S->aux = reinterpret_cast<int*>(p_aux);
+    S->hl = reinterpret_cast<int*>(p_hl);
+    S->ids = reinterpret_cast<int32_t*>(p_ids);
+    S->bad = reinterpret_cast<int*>(p_bad);
+    S->used = p_used;
+    S->newf = p_newf;
+    S->cold = p_cold;
+  }
+  return o;
+}
 
 // Eviction order of an occupied slot (lower = evicted first): recency stamp
 // (LRU), insertion stamp (FIFO), (steps used, insertion stamp) (LFU),
@@ -208,7 +263,7 @@ __device__ __forceinline__ unsigned long long block_reduce_u64(unsigned long lon
 
 // One layer step's bookkeeping by the calling CTA (blockDim.x >= E, a multiple
 // of 32; do_route needs T <= 64).
-__device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
+__device__ __forceinline__ void prepare_body(const PrepArgs& a, const PrepSmem& S) {
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;   // >= E, a multiple of 32
   const int E = a.E, N = a.N;
@@ -239,7 +294,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
     S.used[q] = 0;
   }
   if (tid - l0 >= 0 && tid - l0 < ST_COUNT) S.stats[tid - l0] = a.st->stats[tid - l0];
-  if (tid == 0) S.bad = 0;
+  if (tid == 0) *S.bad = 0;
   if (a.do_route) {
     for (int t = tid >> 5; t < a.T; t += nthr / 32)
       route_dispatch(a.logits + (size_t)t * E, E, a.k, a.renorm, a.ids + (size_t)t * a.k,
@@ -248,11 +303,11 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, PrepSmem& S) {
   __syncthreads();
   for (int i = tid; i < n_ids; i += nthr) {
     const int e = ids_in_smem ? S.ids[i] : a.ids[i];
-    if ((unsigned)e >= (unsigned)E) S.bad = 1;
+    if ((unsigned)e >= (unsigned)E) *S.bad = 1;
     else atomicAdd(&S.nsel[e], 1);
   }
   __syncthreads();
-  if (S.bad) {
+  if (*S.bad) {
     // Reject the whole step: state untouched, every assignment skipped.
     if (tid == 0) {
       atomicExch(a.err, DEVERR_BAD_ID);
