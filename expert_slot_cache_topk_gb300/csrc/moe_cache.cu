@@ -99,6 +99,9 @@ struct moe_cache {
   uint8_t* xs_d[2] = {nullptr, nullptr};
   float* logits_stage_d = nullptr;
   cudaStream_t copy_stream = nullptr;
+  cudaStream_t cap_stream = nullptr;            // capture stream of the host-buffer model step
+  std::vector<cudaGraphExec_t> step_graph;      // [maxT + 1]: all layers of a T-token step, captured once
+  std::vector<unsigned long long> step_graph_launches;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_sync = nullptr;
   int copy_mode = MOE_COPY_UVA;
   int copy_grid = 0;
@@ -521,6 +524,9 @@ void free_all(moe_cache* c) {
     for (auto e : p.beg) cudaEventDestroy(e);
     for (auto e : p.end) cudaEventDestroy(e);
   }
+  for (cudaGraphExec_t g : c->step_graph)
+    if (g) cudaGraphExecDestroy(g);
+  if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
   if (c->ev_fork) cudaEventDestroy(c->ev_fork);
   if (c->ev_join) cudaEventDestroy(c->ev_join);
   if (c->ev_sync) cudaEventDestroy(c->ev_sync);
@@ -636,6 +642,8 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   c->I = g.inter;
   c->N = g.slots_per_layer;
   c->maxT = g.max_tokens;
+  c->step_graph.assign((size_t)c->maxT + 1, nullptr);
+  c->step_graph_launches.assign((size_t)c->maxT + 1, 0ull);
   c->wd = g.wdtype;
   c->Be = w13 + w2 + s13 + s2;
   c->off_w2 = w13;
@@ -908,6 +916,46 @@ moe_status moe_expert_mlp(int wdtype, int hidden, int inter, int top_k, const vo
   return MOE_OK;
 }
 
+namespace {
+
+// Every layer of a T-token step, from xs_d[0] and logits_stage_d; the result
+// lands in xs_d[L & 1].
+moe_status run_layers(moe_cache* c, int T, moe_stream_t stream) {
+  int cur = 0;
+  for (int l = 0; l < c->L; ++l) {
+    moe_status st = moe_forward(c, l, c->xs_d[cur], c->logits_stage_d + (size_t)l * T * c->E, T,
+                                c->xs_d[cur ^ 1], MOE_FWD_RESIDUAL, stream);
+    if (st != MOE_OK) return st;
+    cur ^= 1;
+  }
+  return MOE_OK;
+}
+
+moe_status capture_step_graph(moe_cache* c, int T) {
+  if (!c->cap_stream) CK(c, cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
+  const unsigned long long l0 = c->launches;
+  CK(c, cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+  const moe_status st = run_layers(c, T, (moe_stream_t)c->cap_stream);
+  cudaGraph_t g = nullptr;
+  const cudaError_t ce = cudaStreamEndCapture(c->cap_stream, &g);
+  c->step_graph_launches[T] = c->launches - l0;
+  c->launches = l0;
+  if (st != MOE_OK) {
+    if (g) cudaGraphDestroy(g);
+    return st;
+  }
+  if (ce != cudaSuccess) return cuda_fail(c, ce, "capturing the model step");
+  const cudaError_t ie = cudaGraphInstantiate(&c->step_graph[T], g, 0);
+  cudaGraphDestroy(g);
+  if (ie != cudaSuccess) {
+    c->step_graph[T] = nullptr;
+    return cuda_fail(c, ie, "instantiating the model step graph");
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
 moe_status moe_model_step_host(moe_cache_t* c, const void* x_h, const float* logits_h, int T,
                                void* y_h, int timeout_ms, moe_stream_t stream) {
   if (!c) return fail(nullptr, MOE_EINVAL, "null handle");
@@ -920,12 +968,20 @@ moe_status moe_model_step_host(moe_cache_t* c, const void* x_h, const float* log
   CK(c, cudaMemcpyAsync(c->xs_d[0], x_h, xb, cudaMemcpyHostToDevice, s));
   CK(c, cudaMemcpyAsync(c->logits_stage_d, logits_h, (size_t)c->L * T * c->E * sizeof(float),
                         cudaMemcpyHostToDevice, s));
-  int cur = 0;
-  for (int l = 0; l < c->L; ++l) {
-    moe_status st = moe_forward(c, l, c->xs_d[cur], c->logits_stage_d + (size_t)l * T * c->E, T,
-                                c->xs_d[cur ^ 1], MOE_FWD_RESIDUAL, stream);
+  // the layers run from the staged x / logits: replayed from a graph captured
+  // at the first call with this T (MEMCPY mode takes a host decision per
+  // layer and per-launch timing records host-side events, so both run eagerly)
+  const int cur = c->L & 1;
+  if (c->copy_mode != MOE_COPY_MEMCPY && !c->timing_on) {
+    if (!c->step_graph[T]) {
+      moe_status st = capture_step_graph(c, T);
+      if (st != MOE_OK) return st;
+    }
+    CK(c, cudaGraphLaunch(c->step_graph[T], s));
+    c->launches += c->step_graph_launches[T];
+  } else {
+    moe_status st = run_layers(c, T, (moe_stream_t)s);
     if (st != MOE_OK) return st;
-    cur ^= 1;
   }
   CK(c, cudaMemcpyAsync(y_h, c->xs_d[cur], xb, cudaMemcpyDeviceToHost, s));
   CK(c, cudaEventRecord(c->ev_sync, s));
