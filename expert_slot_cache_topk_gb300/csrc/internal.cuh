@@ -68,6 +68,7 @@ struct PrepArgs {
   int32_t* slot_expert;              // [N]
   long long* slot_stamp;             // [N]
   int32_t* slot_aux;                 // [N]: LFU steps used, SLRU segment (1 = protected)
+  unsigned* ring_cnt;                // [2 * MOE_MAX_TOPK] or null: zeroed (copy counts of the next MLP)
   int policy;                        // moe_evict_policy
   LayerState* st;
   RecHdr* hdr;
@@ -118,6 +119,12 @@ struct MlpArgs {
   const unsigned long long* src_ptr;
   int readthrough;
   unsigned long long tail_off, tail_bytes;
+  // Staged decode kernel with read-through: a copier warp per CTA moves the
+  // pending blocks (blk_bytes each) from src_ptr into their slots in chunks,
+  // counting landed chunks per assignment in copy_cnt[j] (w13 + gate/up
+  // scales) and copy_cnt[MOE_MAX_TOPK + j] (all); prepare zeroes the counts.
+  unsigned* copy_cnt;
+  unsigned long long blk_bytes;
   // Device addresses [host_lo, host_hi) are the mapped pinned backing store:
   // the staged decode kernel reads blocks there with plain loads, never with
   // bulk copies (0, 0 = no host blocks).

@@ -7,7 +7,7 @@
 // "Run MoE models exceeding VRAM via expert CPU offloading with GPU cache",
 // "How it works": the experts run on slot buffers through remapped ids).
 //
-// One persistent CTA per SM, cooperative launch, nine warps:
+// One persistent CTA per SM, cooperative launch, ten warps:
 //   * warp 0 (producer) walks this CTA's share of the work -- first its run
 //     of gate/up row pairs (expert-major), then its output rows -- and for
 //     every stage issues cp.async.bulk copies of the weight rows that live in
@@ -15,12 +15,16 @@
 //   * warps 1..8 (consumers) take every stage in order: up stages produce h,
 //     then all CTAs meet at a grid barrier (h complete), then down stages
 //     produce y.  The producer never waits for the grid barrier, so W2 rows
-//     keep streaming into the ring while the grid synchronises.
-// Rows of blocks in mapped host memory (cold experts; missed experts read
-// through in the same step, "Running 125B MoE on Two 32 GB Cards", section 2:
-// the GPU reads host rows through a UVA view) are not bulk-copied: the
-// consumers read them with plain 16-byte loads, and a read-through row is
-// also stored into the expert's slot.
+//     keep streaming into the ring while the grid synchronises;
+//   * warp 9 (copier) moves the blocks of experts missed in this step from
+//     pinned host memory into their slots ("Running 125B MoE on Two 32 GB
+//     Cards", section 2: the GPU reads host rows through a UVA view), in
+//     chunks spread over the grid, counting landed chunks per expert.  The
+//     producer takes a missed expert's items last and issues their bulk
+//     copies (from the slot) once the chunks they need are counted, so the
+//     host-link transfer overlaps the HBM-resident experts' work.
+// Rows of blocks that stay in mapped host memory (cold experts) are not
+// bulk-copied: the consumers read them with plain 16-byte loads.
 //
 // The consumer warps keep the token's activations in registers (x in the up
 // phase, one part of h in the down phase; see RingTile), so shared memory
@@ -50,7 +54,10 @@ namespace {
 using namespace mlp;
 
 constexpr int kConsumers = 8;                       // consumer warps
-constexpr int kRingThreads = 32 * (1 + kConsumers);
+constexpr int kRingThreads = 32 * (2 + kConsumers);  // producer, consumers, copier
+constexpr int kCopierWarp = 1 + kConsumers;
+constexpr unsigned long long kCopyChunk = 16384;    // copier: bytes per counted chunk
+constexpr int kCopyBatch = 16;                      // copier: 16-byte loads per lane in flight
 constexpr int kMaxStages = 12;
 constexpr int kMaxRows = 64;                        // output rows per CTA whose residual is kept in shared memory
 constexpr int kHRep = 8;                            // copies of h in global memory (read spread over L2)
@@ -81,6 +88,7 @@ struct RingShared {
   float gu[kMaxStages][kConsumers / 2][2]; // up, half-size items: gate / up sums of each pair
   int cnt[kMaxStages][kConsumers / 2];     // up, half-size items: rows of the pair finished
   int stop;                                // set when a wait ran out: skip the rest
+  int jorder[MOE_MAX_TOPK];                // producer: assignments in item order (pending ones last)
 };
 
 struct RingCfg {
@@ -152,6 +160,21 @@ __device__ __forceinline__ unsigned long long evict_first_policy() {
 __device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(src)), "r"(bytes)
                : "memory");
+}
+// true once *p >= target (acquire); false after kWaitNs
+__device__ __forceinline__ bool wait_count(const unsigned* p, unsigned target) {
+  unsigned long long t0 = 0ull;
+  for (unsigned it = 0;; ++it) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if (it == 0) t0 = global_ns();
+    else if (global_ns() - t0 > kWaitNs) return false;
+    __nanosleep(100);
+  }
+}
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
@@ -510,6 +533,74 @@ __device__ __forceinline__ void down_rows(const MlpArgs& a, const RingShared& S,
   }
 }
 
+// ------------------------------------------------------------- copier
+// A pending block is copied in chunks of at most kCopyChunk bytes, phase A
+// first (w13, then the gate/up scales: what the up items read), then phase B
+// (w2, then the down scales).
+__device__ __forceinline__ int chunk_count(unsigned long long bytes) {
+  return (int)((bytes + kCopyChunk - 1) / kCopyChunk);
+}
+__device__ __forceinline__ int phase_chunks(const MlpArgs& a, bool b) {
+  return b ? chunk_count(a.off_s13 - a.off_w2) + chunk_count(a.blk_bytes - a.off_s2)
+           : chunk_count(a.off_w2) + chunk_count(a.off_s2 - a.off_s13);
+}
+// byte range [lo, hi) of chunk c of phase b
+__device__ __forceinline__ void chunk_range(const MlpArgs& a, bool b, int c, unsigned long long* lo,
+                                            unsigned long long* hi) {
+  const unsigned long long r0 = b ? a.off_w2 : 0ull, r0e = b ? a.off_s13 : a.off_w2;
+  const unsigned long long r1 = b ? a.off_s2 : a.off_s13, r1e = b ? a.blk_bytes : a.off_s2;
+  const int n0 = chunk_count(r0e - r0);
+  const unsigned long long base = c < n0 ? r0 : r1, end = c < n0 ? r0e : r1e;
+  *lo = base + (unsigned long long)(c < n0 ? c : c - n0) * kCopyChunk;
+  *hi = *lo + kCopyChunk < end ? *lo + kCopyChunk : end;
+}
+
+// Copier warp: the chunks of the pending blocks, spread over the grid (chunk
+// b, b + G, ... of the global list: every phase A chunk of every pending
+// assignment, then every phase B chunk), host -> slot with plain 16-byte
+// loads and stores; each landed chunk is counted with a release add.
+__device__ __forceinline__ void copier(const MlpArgs& a, const RingShared& S, int lane) {
+  // the same blocks the producer waits for (pending, in HBM, 16-byte aligned)
+  const unsigned long long b = lane < a.k ? S.base[lane] : 0ull;
+  const unsigned pend = __ballot_sync(
+      kFull, lane < a.k && a.pending[lane] != 0 && b != 0ull && !in_host(a, b) && (b & 15ull) == 0ull);
+  if (pend == 0u) return;
+  const long long np = __popc(pend);
+  const int nA = phase_chunks(a, false), nB = phase_chunks(a, true);
+  const long long total = np * (nA + nB);
+  for (long long ci = blockIdx.x; ci < total; ci += gridDim.x) {
+    const bool pb = ci >= np * nA;
+    const long long cc = pb ? ci - np * nA : ci;
+    const int per = pb ? nB : nA;
+    const int pj = (int)(cc / per), c = (int)(cc - (long long)pj * per);
+    const int j = nth_set_bit(pend, pj);
+    unsigned long long lo, hi;
+    chunk_range(a, pb, c, &lo, &hi);
+    const uint4* src = reinterpret_cast<const uint4*>(a.src_ptr[j] + lo);
+    uint4* dst = reinterpret_cast<uint4*>(S.base[j] + lo);
+    const int nv = (int)((hi - lo) / 16ull);
+    for (int v0 = 0; v0 < nv; v0 += 32 * kCopyBatch) {
+      uint4 v[kCopyBatch];
+#pragma unroll
+      for (int u = 0; u < kCopyBatch; ++u) {
+        const int q = v0 + lane + 32 * u;
+        if (q < nv) v[u] = __ldcs(src + q);
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyBatch; ++u) {
+        const int q = v0 + lane + 32 * u;
+        if (q < nv) dst[q] = v[u];
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+      if (!pb) red_release_add(a.copy_cnt + j, 1u);
+      red_release_add(a.copy_cnt + MOE_MAX_TOPK + j, 1u);
+    }
+  }
+}
+
 // ------------------------------------------------------------- producer
 // Items of CTA b of G: up items = groups of P = up_pairs consecutive row
 // pairs of one assignment, groups b, b + G, b + 2 G, ... of the NG = k * I / P
@@ -550,15 +641,27 @@ __device__ __forceinline__ void produce(const MlpArgs& a, const RingCfg& rc, Rin
   // experts that are not bulk-copied: no block, host blocks, blocks filled by
   // read-through in this step, or (defensively) blocks not 16-byte aligned
   const unsigned long long myb = lane < a.k ? S.base[lane] : 0ull;
-  const bool plain = lane < a.k && (myb == 0ull || in_host(a, myb) || (myb & 15ull) != 0ull ||
-                                    (a.readthrough && a.pending[lane] != 0));
+  // with the copier, a pending block is bulk-copied from its slot once its
+  // chunks have landed; without it, the consumers read it through
+  const bool cp_mode = a.readthrough && a.copy_cnt != nullptr;
+  const bool pend = lane < a.k && a.readthrough && a.pending[lane] != 0;
+  const bool plain = lane < a.k && (myb == 0ull || in_host(a, myb) || (myb & 15ull) != 0ull || (pend && !cp_mode));
   const unsigned plain_mask = __ballot_sync(kFull, plain);
   const unsigned k_mask = a.k >= 32 ? kFull : ((1u << a.k) - 1u);
   const int n_ring = __popc(k_mask & ~plain_mask);
+  const unsigned wait_mask = cp_mode ? __ballot_sync(kFull, pend && !plain) : 0u;
+  // item order: the assignments that wait for the copier come last
+  if (lane < a.k) {
+    const unsigned lt = (1u << lane) - 1u, early = k_mask & ~wait_mask;
+    S.jorder[(wait_mask >> lane) & 1u ? __popc(early) + __popc(wait_mask & lt) : __popc(early & lt)] = lane;
+  }
+  __syncwarp();
+  const int nA = cp_mode ? phase_chunks(a, false) : 0, nAll = cp_mode ? nA + phase_chunks(a, true) : 0;
+  unsigned landed = 0u;   // assignments whose phase A chunks have all landed
   const unsigned long long pol_first = evict_first_policy();
   int i = 0;
   for (; i < w.n_items; ++i) {
-    if (i == w.n_up && w.n_items - w.n_up > NS && lane < a.k && !plain) {
+    if (i == w.n_up && w.n_items - w.n_up > NS && lane < a.k && !plain && !((wait_mask >> lane) & 1u)) {
       // the W2 rows of the down items that wait for a free stage: into L2 now,
       // while the grid meets, so that their copies after the barrier are short
       const int nr0 = w.n0 + NS * rc.down_rows;
@@ -581,8 +684,23 @@ __device__ __forceinline__ void produce(const MlpArgs& a, const RingCfg& rc, Rin
     }
     if (i < w.n_up) {
       const int gg = w.g0 + i * w.gstride;
-      const int j = gg / gpe;
-      const int p0 = (gg - j * gpe) * P;
+      const int jj = gg / gpe;
+      const int p0 = (gg - jj * gpe) * P;
+      const int j = S.jorder[jj];
+      if ((wait_mask >> j) & 1u & ~(landed >> j)) {
+        // the block's w13 (and gate/up scales) must be in its slot first
+        bool got = true;
+        if (lane == 0) got = wait_count(a.copy_cnt + j, (unsigned)nA);
+        if (!__shfl_sync(kFull, got, 0)) {
+          if (lane == 0) {
+            atomicExch(err, DEVERR_RING);
+            *reinterpret_cast<volatile int*>(&S.stop) = 1;
+          }
+          break;
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");   // copier stores -> bulk copy reads
+        landed |= 1u << j;
+      }
       const unsigned long long blk = __shfl_sync(kFull, myb, j);
       const bool pl = (plain_mask >> j) & 1u;
       const unsigned src = blk == 0ull ? SRC_NONE : (pl ? SRC_PLAIN : SRC_RING);
@@ -603,6 +721,18 @@ __device__ __forceinline__ void produce(const MlpArgs& a, const RingCfg& rc, Rin
         mbar_arrive(full);
       }
     } else {
+      if (i == w.n_up && wait_mask != 0u) {
+        // every pending block whole in its slot before its W2 rows are read
+        const bool got = !((wait_mask >> lane) & 1u) || wait_count(a.copy_cnt + MOE_MAX_TOPK + lane, (unsigned)nAll);
+        if (!__all_sync(kFull, got)) {
+          if (lane == 0) {
+            atomicExch(err, DEVERR_RING);
+            *reinterpret_cast<volatile int*>(&S.stop) = 1;
+          }
+          break;
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
       const int n = w.n0 + (i - w.n_up) * rc.down_rows;
       const int nr = min(rc.down_rows, w.n1 - n);
       if (lane == 0) S.desc[s] = RingDesc{1, 0, n, nr, plain_mask};
@@ -658,7 +788,7 @@ __device__ __forceinline__ void consume(const MlpArgs& a, const RingCfg& rc, Rin
   // scales) into their slots, 4 KiB per task, an equal share per CTA.  They
   // complete before the grid barrier, so the down items may read them from
   // the slots.
-  if (a.readthrough) {
+  if (a.readthrough && a.copy_cnt == nullptr) {
     const unsigned pend = __ballot_sync(kFull, lane < a.k && a.pending[lane] != 0 && S.base[lane] != 0ull);
     if (pend) {
       const unsigned long long cpe = (a.tail_bytes + 4095ull) / 4096ull;
@@ -822,7 +952,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_mlp_ring(MlpArgs a, RingCfg
   }
   __syncthreads();
   if (warp == 0) produce<F>(a, rc, S, ring, lane, err);
-  else consume<F>(a, rc, S, ring, bar, err, warp - 1, lane);
+  else if (warp == kCopierWarp) {
+    if (a.readthrough && a.copy_cnt != nullptr) copier(a, S, lane);
+  } else {
+    consume<F>(a, rc, S, ring, bar, err, warp - 1, lane);
+  }
 }
 
 // ------------------------------------------------------------------ host

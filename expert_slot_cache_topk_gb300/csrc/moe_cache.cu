@@ -94,6 +94,7 @@ struct moe_cache {
   int* err_d = nullptr;
   int* verify_d = nullptr;
   GridBar* bar_d = nullptr;       // grid barrier of the fused MLP kernel
+  unsigned* ring_cnt_d = nullptr; // [2 * MOE_MAX_TOPK] landed-chunk counts of the staged kernel's copier
   RecHdr* hdr_h = nullptr;        // pinned mirror for MEMCPY mode
   int32_t* lists_h = nullptr;
   uint8_t* xs_d[2] = {nullptr, nullptr};
@@ -229,6 +230,7 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
   a.slot_expert = c->slot_expert_d + (size_t)layer * c->N;
   a.slot_stamp = c->slot_stamp_d + (size_t)layer * c->N;
   a.slot_aux = c->slot_aux_d + (size_t)layer * c->N;
+  a.ring_cnt = c->ring_cnt_d;
   a.policy = c->cfg.evict_policy;
   a.st = c->state_d + layer;
   a.hdr = c->hdr_d + layer;
@@ -319,6 +321,8 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
     m.phase = -1;
     m.tail_off = c->off_w2;
     m.tail_bytes = c->Be - c->off_w2;
+    m.copy_cnt = c->ring_cnt_d;
+    m.blk_bytes = c->Be;
     const int ti = tm_begin(c, TM_UP, s);
     int nl = 1;
     const cudaError_t fe = launch_layer_mlp(c, m, s, &nl);
@@ -533,7 +537,7 @@ void free_all(moe_cache* c) {
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->fstack_d, c->counts_d, c->slot_map_d, c->slot_expert_d,
                  c->slot_stamp_d, c->slot_aux_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
-                 c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->tm_miss_d, c->xs_d[0], c->xs_d[1],
+                 c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->ring_cnt_d, c->tm_miss_d, c->xs_d[0], c->xs_d[1],
                  c->logits_stage_d, c->order_d, c->tiles_d, c->ntiles_d, c->gout_d, c->seq_d, c->ready_d};
   for (void* p : dev)
     if (p) cudaFree(p);
@@ -719,6 +723,8 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   CKC(dmalloc((void**)&c->h_d, h_floats * sizeof(float)));
   CKC(dmalloc((void**)&c->err_d, sizeof(int)));
   CKC(dmalloc((void**)&c->bar_d, sizeof(GridBar)));
+  CKC(dmalloc((void**)&c->ring_cnt_d, 2 * MOE_MAX_TOPK * sizeof(unsigned)));
+  CKC(cudaMemset(c->ring_cnt_d, 0, 2 * MOE_MAX_TOPK * sizeof(unsigned)));
   CKC(dmalloc((void**)&c->seq_d, sizeof(unsigned)));
   CKC(dmalloc((void**)&c->ready_d, (size_t)E * sizeof(unsigned)));
   // zeroed once: the prepare counter never goes back (not even on reset), so
