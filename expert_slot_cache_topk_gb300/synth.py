@@ -109,7 +109,9 @@ def expert_layout(wdtype: str, hidden: int, inter: int) -> dict:
     w13 is [2*inter, hidden] (rows [0, inter) gate, [inter, 2*inter) up),
     w2 is [hidden, inter], both row-major.  INT4: two weights per byte along
     the row, low nibble = even column; s13 [2*inter, hidden/128] and
-    s2 [hidden, inter/128] bf16 scales.
+    s2 [hidden, inter/128] bf16 scales.  FP8: one E4M3 byte per weight;
+    s13 = float32 [gate scale, up scale] and s2 = float32 [down scale], each
+    zero-padded to 16 bytes.
     """
     H, I = hidden, inter
     if wdtype == "f32":
@@ -121,6 +123,10 @@ def expert_layout(wdtype: str, hidden: int, inter: int) -> dict:
             raise ValueError("int4g128 needs hidden and inter divisible by 128")
         w13, w2 = 2 * I * H // 2, H * I // 2
         s13, s2 = 2 * I * (H // 128) * 2, H * (I // 128) * 2
+    elif wdtype == "fp8":
+        if H % 16 or I % 16:
+            raise ValueError("fp8 needs hidden and inter divisible by 16")
+        w13, w2, s13, s2 = 2 * I * H, H * I, 16, 16
     else:
         raise ValueError(wdtype)
     return {"w13": (0, w13), "w2": (w13, w2), "s13": (w13 + w2, s13),
@@ -179,6 +185,38 @@ def _quantize_int4_g128(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return packed, s_bits
 
 
+_E4M3_POS = None
+
+
+def _e4m3_positive_values() -> np.ndarray:
+    """Magnitudes of the finite E4M3 codes 0x00..0x7E (increasing with the code)."""
+    global _E4M3_POS
+    if _E4M3_POS is None:
+        v = []
+        for code in range(0x7F):
+            exp, man = code >> 3, code & 7
+            v.append(man * 2.0 ** -9 if exp == 0 else (8 + man) * 2.0 ** (exp - 10))
+        _E4M3_POS = np.array(v, dtype=np.float64)
+    return _E4M3_POS
+
+
+def _quantize_fp8(w: np.ndarray) -> tuple[np.ndarray, np.float32]:
+    """Per-tensor E4M3 (generator only): s = float32(max|w| / 448), each
+    weight w / s rounded to the nearest E4M3 value, ties to the even code."""
+    amax = float(np.abs(w).max())
+    s = np.float32(amax / 448.0) if amax > 0 else np.float32(1.0)
+    x = np.abs(w.astype(np.float64) / float(s)).reshape(-1)
+    pos = _e4m3_positive_values()
+    hi = np.clip(np.searchsorted(pos, x), 1, len(pos) - 1)
+    lo = hi - 1
+    dlo, dhi = x - pos[lo], pos[hi] - x
+    code = np.where(dhi < dlo, hi, lo)
+    code = np.where(dhi == dlo, np.where(lo % 2 == 0, lo, hi), code)
+    code = np.where(x >= pos[-1], len(pos) - 1, code).astype(np.uint8)
+    code |= np.where(w.reshape(-1) < 0, np.uint8(0x80), np.uint8(0))
+    return code.reshape(w.shape), s
+
+
 def expert_block(w: Workload, layer: int, expert: int, out: Optional[np.ndarray] = None) -> np.ndarray:
     """The canonical byte block of one expert (uint8, expert_layout(...)['total'] bytes)."""
     H, I = w.hidden, w.inter
@@ -196,6 +234,20 @@ def expert_block(w: Workload, layer: int, expert: int, out: Optional[np.ndarray]
         out[o:o + n] = _f32_to_bf16_bits(_normal_f32(g, 2 * I * H, WEIGHT_STD)).view(np.uint8)
         o, n = lay["w2"]
         out[o:o + n] = _f32_to_bf16_bits(_normal_f32(g, H * I, WEIGHT_STD)).view(np.uint8)
+    elif w.wdtype == "fp8":
+        w13 = _normal_f32(g, 2 * I * H, WEIGHT_STD).reshape(2 * I, H)
+        qg, sg = _quantize_fp8(w13[:I])
+        qu, su = _quantize_fp8(w13[I:])
+        qd, sd = _quantize_fp8(_normal_f32(g, H * I, WEIGHT_STD).reshape(H, I))
+        o, n = lay["w13"]
+        out[o:o + n] = np.concatenate([qg.reshape(-1), qu.reshape(-1)])
+        o, n = lay["w2"]
+        out[o:o + n] = qd.reshape(-1)
+        for key, vals in (("s13", [sg, su]), ("s2", [sd])):
+            o, n = lay[key]
+            pad = np.zeros(n // 4, dtype=np.float32)
+            pad[: len(vals)] = vals
+            out[o:o + n] = pad.view(np.uint8)
     else:
         q13, s13 = _quantize_int4_g128(_normal_f32(g, 2 * I * H, WEIGHT_STD).reshape(2 * I, H))
         q2, s2 = _quantize_int4_g128(_normal_f32(g, H * I, WEIGHT_STD).reshape(H, I))

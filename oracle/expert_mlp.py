@@ -19,6 +19,14 @@ Readings where the pages are open
   (q - 8) * scale with one bf16 scale per 128 consecutive columns and no zero
   point.  This is the reading that reproduces the page's 2.417 MiB exactly.
 * y[t] = sum over j (in j order) of w[t, j] * W2_e (h_e), all in float64.
+* FP8 per tensor (vLLM PR #37190 supports "BF16 + FP8 per-tensor" weights,
+  with scale buffers copied into the slot together with the weights): one
+  byte per weight in the OCP E4M3 encoding (sign, 4 exponent bits with bias 7,
+  3 mantissa bits; exponent field 0 = subnormal 2^-6 * m / 8; no infinities;
+  S.1111.111 = NaN), value = decoded byte * the tensor's float32 scale, with
+  three tensors per expert: gate (w13 rows [0, I)), up (rows [I, 2I)) and
+  down (w2).  s13 = [gate scale, up scale] and s2 = [down scale], each part
+  zero-padded to 16 bytes.
 
 Canonical block layout: [w13 | w2 | s13 | s2], each part row-major.
 """
@@ -37,6 +45,8 @@ def expert_nbytes(wdtype: str, H: int, I: int) -> dict:
     elif wdtype == "int4g128":
         parts = {"w13": (2 * I) * (H // 2), "w2": H * (I // 2),
                  "s13": (2 * I) * (H // 128) * 2, "s2": H * (I // 128) * 2}
+    elif wdtype == "fp8":
+        parts = {"w13": 2 * I * H, "w2": H * I, "s13": 16, "s2": 16}
     else:
         raise ValueError(wdtype)
     parts["total"] = parts["w13"] + parts["w2"] + parts["s13"] + parts["s2"]
@@ -71,6 +81,23 @@ def dequant_int4_g128(packed: np.ndarray, scale_bits: np.ndarray, rows: int, K: 
     return (q - 8).astype(np.float64) * s[:, col_group]
 
 
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """OCP E4M3 bytes -> float64, from the format's definition (exact)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    out = sign * mag
+    out[(c & 0x7F) == 0x7F] = np.nan
+    return out
+
+
+def dequant_fp8(codes: np.ndarray, scale: float, rows: int, K: int) -> np.ndarray:
+    """E4M3 bytes [rows, K] times one per-tensor float32 scale -> float64 [rows, K]."""
+    return e4m3_to_f64(np.asarray(codes).reshape(rows, K)) * float(np.float32(scale))
+
+
 def dequant_expert(block: np.ndarray, wdtype: str, H: int, I: int):
     """One expert block -> (w13 float64 [2I, H], w2 float64 [H, I])."""
     parts = split_block(block, wdtype, H, I)
@@ -80,6 +107,12 @@ def dequant_expert(block: np.ndarray, wdtype: str, H: int, I: int):
     elif wdtype == "bf16":
         w13 = bf16_bits_to_f64(parts["w13"].view(np.uint16)).reshape(2 * I, H)
         w2 = bf16_bits_to_f64(parts["w2"].view(np.uint16)).reshape(H, I)
+    elif wdtype == "fp8":
+        s13 = parts["s13"].view(np.float32)
+        s2 = parts["s2"].view(np.float32)
+        w13 = np.concatenate([dequant_fp8(parts["w13"][: I * H], s13[0], I, H),
+                              dequant_fp8(parts["w13"][I * H:], s13[1], I, H)])
+        w2 = dequant_fp8(parts["w2"], s2[0], H, I)
     else:
         w13 = dequant_int4_g128(parts["w13"], parts["s13"].view(np.uint16), 2 * I, H)
         w2 = dequant_int4_g128(parts["w2"], parts["s2"].view(np.uint16), H, I)
