@@ -127,6 +127,12 @@ class ClockSampler:
 # workload
 # ---------------------------------------------------------------------------
 
+# arithmetic of the decode path per weight format: weights decoded to f32 in
+# registers, f32 accumulation, bf16 activations (f32 for f32 weights)
+DTYPE_NAME = {"bf16": "bf16", "f32": "f32", "fp8": "fp8_e4m3 weights, bf16 activations",
+              "int4g128": "int4_g128 weights, bf16 activations"}
+
+
 def workload_desc(w) -> str:
     return (f"{w.name}-shaped decode: {w.layers} MoE layers x {w.experts} experts, top-{w.top_k}, "
             f"hidden {w.hidden}, expert inter {w.inter}, {w.wdtype} weights, {w.slots} slots/layer, "
@@ -499,7 +505,7 @@ def run_ours(args, w):
         line = {
             "metric": METRIC, "value": all_tokens / max_sec, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * max_sec / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.wdtype],
             "data": "synthetic (seeded Zipf routing with reuse; N(0,0.02) weights)",
             "config": {"workload": workload_desc(w), "tokens_per_step": w.tokens,
                        "copy_mode": info["copy_mode_name"], "graph": use_graph,
@@ -554,6 +560,8 @@ def main():
     ap.add_argument("--copy-mode", default="auto", choices=["auto", "uva", "memcpy", "fused"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling case)")
     ap.add_argument("--slots", type=int, default=-1, help="override the pool slots per layer (N)")
+    ap.add_argument("--wdtype", default="", choices=["", "f32", "bf16", "int4g128", "fp8"],
+                    help="override the decode workload's weight format")
     ap.add_argument("--clock-ms", type=int, default=100, help="nvidia-smi sampling interval in ms")
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
@@ -569,6 +577,8 @@ def main():
         w = w.with_(layers=args.layers)
     if args.slots >= 0:
         w = w.with_(slots=args.slots)
+    if args.wdtype:
+        w = w.with_(wdtype=args.wdtype)
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -17,8 +17,8 @@ import numpy as np
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoecache.so")
 
-MOE_F32, MOE_BF16, MOE_INT4_G128 = 0, 1, 2
-WDTYPE = {"f32": MOE_F32, "bf16": MOE_BF16, "int4g128": MOE_INT4_G128}
+MOE_F32, MOE_BF16, MOE_INT4_G128, MOE_FP8_E4M3 = 0, 1, 2, 3
+WDTYPE = {"f32": MOE_F32, "bf16": MOE_BF16, "int4g128": MOE_INT4_G128, "fp8": MOE_FP8_E4M3}
 MOE_COPY_AUTO, MOE_COPY_MEMCPY, MOE_COPY_UVA, MOE_COPY_FUSED = 0, 1, 2, 3
 COPY_MODE = {"auto": MOE_COPY_AUTO, "memcpy": MOE_COPY_MEMCPY, "uva": MOE_COPY_UVA,
              "fused": MOE_COPY_FUSED}

@@ -61,6 +61,7 @@ struct UpWarp {
   const uint16_t* sb;
   unsigned long long base;
   int asg, p0;
+  float fsg, fsu, fsd;   // FP8: gate, up and down tensor scales
 
   // task = (pair group, selected assignment), pair-major so that a contiguous
   // task range touches every selected expert
@@ -74,6 +75,12 @@ struct UpWarp {
     const uint8_t* wb = reinterpret_cast<const uint8_t*>(src);
     delta = (long long)(base - src);
     sb = reinterpret_cast<const uint16_t*>(wb + a.off_s13);
+    if (F == MOE_FP8_E4M3 && base != 0ull) {
+      const float* f13 = reinterpret_cast<const float*>(wb + a.off_s13);
+      fsg = __ldcg(f13);
+      fsu = __ldcg(f13 + 1);
+      fsd = __ldcg(reinterpret_cast<const float*>(wb + a.off_s2));
+    }
     const size_t rb = row_bytes<F>(a.H);
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -135,8 +142,16 @@ struct UpWarp {
 #pragma unroll
       for (int p = 0; p < RP; ++p) {
         if (p0 + p < a.I) {
-          const float g = acc[p], u = acc[RP + p];
-          hrow[p0 + p] = base != 0ull ? wa * (g / (1.0f + expf(-g)) * u) : 0.f;
+          float g = acc[p], u = acc[RP + p];
+          if (F == MOE_FP8_E4M3) {
+            // per-tensor scales: gate and up on their dot products; the down
+            // scale folded into h (the down pass mixes experts in one dot)
+            g *= fsg;
+            u *= fsu;
+          }
+          float hv = base != 0ull ? wa * (g / (1.0f + expf(-g)) * u) : 0.f;
+          if (F == MOE_FP8_E4M3) hv *= fsd;
+          hrow[p0 + p] = hv;
         }
       }
     }
@@ -430,6 +445,10 @@ template <>
 struct Tiles<MOE_INT4_G128> {
   static constexpr int RP = 2, UU = 1, UD = 4;
 };
+template <>
+struct Tiles<MOE_FP8_E4M3> {
+  static constexpr int RP = 1, UU = 4, UD = 8;
+};
 
 // Opt a kernel into more than 48 KiB of dynamic shared memory once per size,
 // so launches (also inside stream capture) do not repeat the attribute call.
@@ -555,6 +574,7 @@ cudaError_t mlp_configure(int wdtype, int H, int I, int k) {
     case MOE_F32: return configure_impl<MOE_F32>(H, I, k);
     case MOE_BF16: return configure_impl<MOE_BF16>(H, I, k);
     case MOE_INT4_G128: return configure_impl<MOE_INT4_G128>(H, I, k);
+    case MOE_FP8_E4M3: return configure_impl<MOE_FP8_E4M3>(H, I, k);
   }
   return cudaErrorInvalidValue;
 }
@@ -565,6 +585,7 @@ cudaError_t launch_mlp_up(int wdtype, const MlpArgs& a, cudaStream_t s) {
     case MOE_F32: return up_impl<MOE_F32>(a, s);
     case MOE_BF16: return up_impl<MOE_BF16>(a, s);
     case MOE_INT4_G128: return up_impl<MOE_INT4_G128>(a, s);
+    case MOE_FP8_E4M3: return up_impl<MOE_FP8_E4M3>(a, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -575,6 +596,7 @@ cudaError_t launch_mlp_fused(int wdtype, const MlpArgs& a, GridBar* bar, int* er
     case MOE_F32: return fused_impl<MOE_F32>(a, bar, err, s);
     case MOE_BF16: return fused_impl<MOE_BF16>(a, bar, err, s);
     case MOE_INT4_G128: return fused_impl<MOE_INT4_G128>(a, bar, err, s);
+    case MOE_FP8_E4M3: return fused_impl<MOE_FP8_E4M3>(a, bar, err, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -585,6 +607,7 @@ cudaError_t launch_mlp_down(int wdtype, const MlpArgs& a, cudaStream_t s) {
     case MOE_F32: return down_impl<MOE_F32>(a, s);
     case MOE_BF16: return down_impl<MOE_BF16>(a, s);
     case MOE_INT4_G128: return down_impl<MOE_INT4_G128>(a, s);
+    case MOE_FP8_E4M3: return down_impl<MOE_FP8_E4M3>(a, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -89,6 +89,7 @@ struct RingShared {
   int cnt[kMaxStages][kConsumers / 2];     // up, half-size items: rows of the pair finished
   int stop;                                // set when a wait ran out: skip the rest
   int jorder[MOE_MAX_TOPK];                // producer: assignments in item order (pending ones last)
+  float fsc[MOE_MAX_TOPK][3];              // FP8: gate, up and down tensor scales of each assignment
 };
 
 struct RingCfg {
@@ -254,6 +255,10 @@ template <>
 struct RingTile<MOE_INT4_G128> {
   static constexpr int XM = 3, HM = 2;
 };
+template <>
+struct RingTile<MOE_FP8_E4M3> {
+  static constexpr int XM = 4, HM = 4;
+};
 
 // dot product of one 16-byte weight chunk with EL activations in registers
 template <int F>
@@ -340,8 +345,16 @@ __device__ __forceinline__ void rows_dot(const uint4* const (&row)[NR], const ui
   }
 }
 
+// h = w * silu(g) * u.  FP8: the gate and up tensor scales apply to the dot
+// products, and the down scale is folded into h (a down dot mixes experts).
+template <int F>
 __device__ __forceinline__ float swiglu_h(const RingShared& S, unsigned long long base, int asg, float g, float u) {
-  return base != 0ull ? S.wt[asg] * (g / (1.0f + expf(-g)) * u) : 0.f;
+  if (F == MOE_FP8_E4M3) {
+    g *= S.fsc[asg][0];
+    u *= S.fsc[asg][1];
+  }
+  const float h = base != 0ull ? S.wt[asg] * (g / (1.0f + expf(-g)) * u) : 0.f;
+  return F == MOE_FP8_E4M3 ? h * S.fsc[asg][2] : h;
 }
 
 // Up item of P = d.n row pairs (pairs d.p0 .. d.p0 + P - 1 of assignment
@@ -385,7 +398,7 @@ __device__ __forceinline__ void up_item(const MlpArgs& a, RingShared& S, const R
     }
     // every lane holds the sums: lanes 0..kHRep-1 write one copy of h each
     if (lane < kHRep)
-      a.h[(size_t)lane * a.k * a.I + (size_t)d.asg * a.I + d.p0 + cw] = swiglu_h(S, base, d.asg, v[0], v[1]);
+      a.h[(size_t)lane * a.k * a.I + (size_t)d.asg * a.I + d.p0 + cw] = swiglu_h<F>(S, base, d.asg, v[0], v[1]);
   } else {
     float v[1] = {0.f};
     if (d.src != SRC_NONE) {
@@ -402,7 +415,7 @@ __device__ __forceinline__ void up_item(const MlpArgs& a, RingShared& S, const R
         __threadfence_block();
         const float g = S.gu[s][pr][0], u = S.gu[s][pr][1];
         S.cnt[s][pr] = 0;
-        const float hv = swiglu_h(S, base, d.asg, g, u);
+        const float hv = swiglu_h<F>(S, base, d.asg, g, u);
         for (int r = 0; r < kHRep; ++r) a.h[(size_t)r * a.k * a.I + (size_t)d.asg * a.I + d.p0 + pr] = hv;
       }
     }
@@ -935,6 +948,21 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_mlp_ring(MlpArgs a, RingCfg
   if (threadIdx.x < a.k) {
     S.base[threadIdx.x] = a.asg_ptr[threadIdx.x];
     S.wt[threadIdx.x] = a.w[threadIdx.x];
+    if (F == MOE_FP8_E4M3) {
+      // the block's scales: from its host copy while the copier is still moving it
+      const unsigned long long b = (a.readthrough && a.pending[threadIdx.x] != 0) ? a.src_ptr[threadIdx.x]
+                                                                                  : a.asg_ptr[threadIdx.x];
+      float g = 0.f, u = 0.f, dn = 0.f;
+      if (b != 0ull) {
+        const float* f13 = reinterpret_cast<const float*>(b + a.off_s13);
+        g = __ldcg(f13);
+        u = __ldcg(f13 + 1);
+        dn = __ldcg(reinterpret_cast<const float*>(b + a.off_s2));
+      }
+      S.fsc[threadIdx.x][0] = g;
+      S.fsc[threadIdx.x][1] = u;
+      S.fsc[threadIdx.x][2] = dn;
+    }
   }
   if (a.residual) {
     const Share w = cta_share(a, rc);
@@ -961,21 +989,24 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_mlp_ring(MlpArgs a, RingCfg
 
 // ------------------------------------------------------------------ host
 size_t host_row_bytes(int F, int K) {
-  return F == MOE_F32 ? (size_t)K * 4 : (F == MOE_BF16 ? (size_t)K * 2 : (size_t)K / 2);
+  return F == MOE_F32 ? (size_t)K * 4
+                      : (F == MOE_BF16 ? (size_t)K * 2 : (F == MOE_FP8_E4M3 ? (size_t)K : (size_t)K / 2));
 }
 
 // Stage geometry for a shape, or false if the staged kernel cannot take it.
 bool ring_geometry(int F, int H, int I, int k, RingCfg* rc, size_t* dyn_smem) {
   if (k < 1 || k > MOE_MAX_TOPK || H < 1) return false;
   const size_t rb1 = host_row_bytes(F, H), rb2 = host_row_bytes(F, I);
-  const int el = F == MOE_F32 ? 4 : (F == MOE_BF16 ? 8 : 32);
+  const int el = F == MOE_F32 ? 4 : (F == MOE_BF16 ? 8 : (F == MOE_FP8_E4M3 ? 16 : 32));
   if (H % el || I % el || rb1 % 16 || rb2 % 16) return false;
   const bool q = F == MOE_INT4_G128;
   if (q && (H % 128 || I % 128)) return false;
   // the consumers hold x (H / el chunks) and one part of h (ceil(k * I / el /
   // kParts) chunks) in registers: at most 32 * XM and 32 * HM chunks per warp
-  const int xm = q ? RingTile<MOE_INT4_G128>::XM : RingTile<MOE_BF16>::XM;
-  const int hm = q ? RingTile<MOE_INT4_G128>::HM : RingTile<MOE_BF16>::HM;
+  const int xm = q ? RingTile<MOE_INT4_G128>::XM
+                   : (F == MOE_FP8_E4M3 ? RingTile<MOE_FP8_E4M3>::XM : RingTile<MOE_BF16>::XM);
+  const int hm = q ? RingTile<MOE_INT4_G128>::HM
+                   : (F == MOE_FP8_E4M3 ? RingTile<MOE_FP8_E4M3>::HM : RingTile<MOE_BF16>::HM);
   if (H / el > 32 * xm || (k * I / el + kParts - 1) / kParts > 32 * hm) return false;
   const size_t srb1 = q ? (size_t)(H / 128) * 2 : 0, srb2 = q ? (size_t)(I / 128) * 2 : 0;
   // up items of kConsumers pairs (one pair per warp) while they stay small;
@@ -1079,6 +1110,7 @@ cudaError_t mlp_ring_configure(int wdtype, int H, int I, int k) {
     case MOE_F32: return ring_configure_impl<MOE_F32>(H, I, k);
     case MOE_BF16: return ring_configure_impl<MOE_BF16>(H, I, k);
     case MOE_INT4_G128: return ring_configure_impl<MOE_INT4_G128>(H, I, k);
+    case MOE_FP8_E4M3: return ring_configure_impl<MOE_FP8_E4M3>(H, I, k);
   }
   return cudaErrorInvalidValue;
 }
@@ -1089,6 +1121,7 @@ cudaError_t launch_mlp_ring(int wdtype, const MlpArgs& a, GridBar* bar, int* err
     case MOE_F32: return ring_impl<MOE_F32>(a, bar, err, s);
     case MOE_BF16: return ring_impl<MOE_BF16>(a, bar, err, s);
     case MOE_INT4_G128: return ring_impl<MOE_INT4_G128>(a, bar, err, s);
+    case MOE_FP8_E4M3: return ring_impl<MOE_FP8_E4M3>(a, bar, err, s);
   }
   return cudaErrorInvalidValue;
 }

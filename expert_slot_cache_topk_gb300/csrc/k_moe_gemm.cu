@@ -176,7 +176,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // K = I.  Epilogue: f32 output rows.
 constexpr int kGStagesP = 4;                 // staged K steps
 constexpr int kGAhead = 2;                   // K steps in flight ahead of the MMA
-constexpr int kRawBytes = kTileM * 2 * 16;   // INT4 raw rows of one K step
+constexpr int kRawBytes = kTileM * 2 * 32;   // raw INT4 (16 B per thread) or FP8 (32 B) rows of one K step
 constexpr int kMaxGroups = 64;               // scale groups per row kept in shared memory (K <= 8192)
 
 template <int F, int PH>
@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
   const int items = ntiles * NT;
   const int K = PH == PH_UP ? g.H : g.I;
   const int nk = K / (int)tc::kTileK;
-  const size_t wrb = PH == PH_UP ? (F == MOE_BF16 ? (size_t)g.H * 2 : (size_t)g.H / 2)
-                                 : (F == MOE_BF16 ? (size_t)g.I * 2 : (size_t)g.I / 2);
+  const size_t wrb = F == MOE_BF16 ? (size_t)K * 2 : (F == MOE_FP8_E4M3 ? (size_t)K : (size_t)K / 2);
+  constexpr int kRawPer = F == MOE_FP8_E4M3 ? 32 : 16;   // raw bytes each thread stages per K step
   const int groups = K / 128;          // INT4 scale groups per weight row
   // layout: [stages x (A tile | B tile)] [stages x raw INT4] [128 x groups scales]
   uint8_t* base = smem + ((1024u - (tc::smem_u32(smem) & 1023u)) & 1023u);
@@ -257,6 +257,13 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
       // this item's scales: 128 rows x groups, two threads per row
       for (int q = hh; q < groups; q += 2) sc[r * kMaxGroups + q] = sbase[(size_t)wrow * groups + q];
     }
+    float fsg = 1.f, fsu = 1.f, fsd = 1.f;   // FP8: the expert's gate, up and down tensor scales
+    if (F == MOE_FP8_E4M3 && PH == PH_UP && blk != 0ull) {
+      const float* f13 = reinterpret_cast<const float*>(blk + g.off_s13);
+      fsg = __ldcg(f13);
+      fsu = __ldcg(f13 + 1);
+      fsd = __ldcg(reinterpret_cast<const float*>(blk + g.off_s2));
+    }
     // stage the operands of K step ks (global step gq) into stage gq % kGStagesP
     auto issue = [&](int ks, unsigned gq) {
       const int s = (int)(gq % kGStagesP);
@@ -274,8 +281,12 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
           const uint32_t kk = (uint32_t)((hh * 4 + i) * 8);
           cp_async16(sb_u + tc::tile_offset((uint32_t)r, kk), wrow_p + (size_t)(k0 + kk) * 2, true);
         }
+      } else if (F == MOE_FP8_E4M3) {
+        const uint32_t d0 = tc::smem_u32(raw0 + (size_t)s * kRawBytes + (size_t)tid * kRawPer);
+        cp_async16(d0, wrow_p + (size_t)(k0 + 32 * hh), true);
+        cp_async16(d0 + 16u, wrow_p + (size_t)(k0 + 32 * hh) + 16, true);
       } else {
-        cp_async16(tc::smem_u32(raw0 + (size_t)s * kRawBytes + (size_t)tid * 16),
+        cp_async16(tc::smem_u32(raw0 + (size_t)s * kRawBytes + (size_t)tid * kRawPer),
                    wrow_p + (size_t)(k0 + 32 * hh) / 2, true);
       }
     };
@@ -307,8 +318,27 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
       cp_async_wait<kGAhead>();          // this thread's copies of step ks have landed
       uint8_t* sa = base + (size_t)s * kGStageBytes;
       uint8_t* sbt = sa + kTileBytes;
+      if (F == MOE_FP8_E4M3) {
+        // 32 E4M3 codes -> bf16 (exact); the tensor scales apply in the epilogue
+        const uint4* rq = reinterpret_cast<const uint4*>(raw0 + (size_t)s * kRawBytes + (size_t)tid * kRawPer);
+        const uint4 q0 = rq[0], q1 = rq[1];
+        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t o[4];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint32_t wd = words[2 * i + h2];   // elements 8 i + 4 h2 .. + 3
+            const float2 a = e4m3x2_to_f2(wd), b = e4m3x2_to_f2(wd >> 16);
+            o[2 * h2] = pack_bf16x2(a.x, a.y);
+            o[2 * h2 + 1] = pack_bf16x2(b.x, b.y);
+          }
+          *reinterpret_cast<uint4*>(sbt + tc::tile_offset((uint32_t)r, (uint32_t)((hh * 4 + i) * 8))) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
       if (F == MOE_INT4_G128) {
-        const uint4 qv = *reinterpret_cast<const uint4*>(raw0 + (size_t)s * kRawBytes + (size_t)tid * 16);
+        const uint4 qv = *reinterpret_cast<const uint4*>(raw0 + (size_t)s * kRawBytes + (size_t)tid * kRawPer);
         const float scl = bf16_bits(sc[r * kMaxGroups + ((ks * (int)tc::kTileK) >> 7)]);
         const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
@@ -362,8 +392,8 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
           float hv[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float gg = __uint_as_float(gv[8 * q + e]), uu = __uint_as_float(uv[8 * q + e]);
-            hv[e] = wa * (gg / (1.0f + expf(-gg)) * uu);
+            const float gg = __uint_as_float(gv[8 * q + e]) * fsg, uu = __uint_as_float(uv[8 * q + e]) * fsu;
+            hv[e] = wa * (gg / (1.0f + expf(-gg)) * uu) * fsd;
           }
           uint4 o;
           o.x = pack_bf16x2(hv[0], hv[1]);
@@ -518,7 +548,7 @@ cudaError_t gemm_impl(const MlpArgs& a, const GemmBuffers& b, cudaStream_t s) {
 }  // namespace
 
 bool moe_gemm_supported(int wdtype, int H, int I, int k) {
-  if (wdtype != MOE_BF16 && wdtype != MOE_INT4_G128) return false;
+  if (wdtype != MOE_BF16 && wdtype != MOE_INT4_G128 && wdtype != MOE_FP8_E4M3) return false;
   if (k < 1 || k > MOE_MAX_TOPK) return false;
   if (H % kTileN || I % 64) return false;          // N tiles of the two GEMMs, K tiles of 64
   if (H > 128 * kMaxGroups || I > 128 * kMaxGroups) return false;   // scales of an item in shared memory
@@ -530,6 +560,7 @@ cudaError_t moe_gemm_configure(int wdtype) {
   switch (wdtype) {
     case MOE_BF16: return gemm_configure_impl<MOE_BF16>();
     case MOE_INT4_G128: return gemm_configure_impl<MOE_INT4_G128>();
+    case MOE_FP8_E4M3: return gemm_configure_impl<MOE_FP8_E4M3>();
   }
   return cudaErrorNotSupported;
 }
@@ -541,6 +572,7 @@ cudaError_t launch_moe_gemm(int wdtype, const MlpArgs& a, const GemmBuffers& b, 
   switch (wdtype) {
     case MOE_BF16: return gemm_impl<MOE_BF16>(a, b, s);
     case MOE_INT4_G128: return gemm_impl<MOE_INT4_G128>(a, b, s);
+    case MOE_FP8_E4M3: return gemm_impl<MOE_FP8_E4M3>(a, b, s);
   }
   return cudaErrorNotSupported;
 }

@@ -4,6 +4,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstring>
 #include <cstdint>
 
 #include "internal.cuh"
@@ -27,6 +29,10 @@ struct FmtT<MOE_BF16> {
 template <>
 struct FmtT<MOE_INT4_G128> {
   static constexpr int kElems = 32;
+};
+template <>
+struct FmtT<MOE_FP8_E4M3> {
+  static constexpr int kElems = 16;
 };
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -99,9 +105,36 @@ __device__ __forceinline__ float chunk_dot<MOE_INT4_G128>(const uint4 w,
   return s;
 }
 
+// two E4M3 codes (low byte = lower element) -> two exact floats
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)(two & 0xffffu)));
+  __half2 v;
+  memcpy(&v, &h, 4);
+  return __half22float2(v);
+}
+
+// 16 codes: byte i of 32-bit word j is element 4 j + i.  The per-tensor
+// scale is applied by the caller to the whole row's dot product.
+template <>
+__device__ __forceinline__ float chunk_dot<MOE_FP8_E4M3>(const uint4 w, const float* __restrict__ x) {
+  const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 a = e4m3x2_to_f2(wd[j]), b = e4m3x2_to_f2(wd[j] >> 16);
+    s = fmaf(a.x, x[4 * j], s);
+    s = fmaf(a.y, x[4 * j + 1], s);
+    s = fmaf(b.x, x[4 * j + 2], s);
+    s = fmaf(b.y, x[4 * j + 3], s);
+  }
+  return s;
+}
+
 template <int F>
 __device__ __forceinline__ size_t row_bytes(int K) {
-  return F == MOE_F32 ? (size_t)K * 4 : (F == MOE_BF16 ? (size_t)K * 2 : (size_t)K / 2);
+  return F == MOE_F32 ? (size_t)K * 4
+                      : (F == MOE_BF16 ? (size_t)K * 2 : (F == MOE_FP8_E4M3 ? (size_t)K : (size_t)K / 2));
 }
 
 __device__ __forceinline__ float bf16_bits(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }

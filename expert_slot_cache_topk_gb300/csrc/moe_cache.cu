@@ -47,11 +47,17 @@ bool layout(int wd, int H, int I, size_t* w13, size_t* w2, size_t* s13, size_t* 
       *w13 = 2 * i * h / 2; *w2 = h * i / 2;
       *s13 = 2 * i * (h / 128) * 2; *s2 = h * (i / 128) * 2;
       return true;
+    case MOE_FP8_E4M3:
+      if (H % 16 || I % 16) return false;
+      *w13 = 2 * i * h; *w2 = h * i; *s13 = 16; *s2 = 16;
+      return true;
   }
   return false;
 }
 
-int chunk_elems(int wd) { return wd == MOE_F32 ? 4 : (wd == MOE_BF16 ? 8 : 32); }
+int chunk_elems(int wd) {
+  return wd == MOE_F32 ? 4 : (wd == MOE_BF16 ? 8 : (wd == MOE_FP8_E4M3 ? 16 : 32));
+}
 size_t act_bytes(int wd) { return wd == MOE_F32 ? 4 : 2; }
 
 }  // namespace
@@ -615,9 +621,9 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
     return fail(nullptr, MOE_EINVAL, "need max_tokens >= 1 and max_tokens * top_k <= 65535");
   size_t w13, w2, s13, s2;
   if (g.hidden <= 0 || g.inter <= 0 || !layout(g.wdtype, g.hidden, g.inter, &w13, &w2, &s13, &s2))
-    return fail(nullptr, MOE_EINVAL, "bad wdtype or shape (int4 needs hidden, inter multiples of 128)");
+    return fail(nullptr, MOE_EINVAL, "bad wdtype or shape (int4 needs hidden, inter multiples of 128; fp8 of 16)");
   if (g.hidden % chunk_elems(g.wdtype) || g.inter % chunk_elems(g.wdtype))
-    return fail(nullptr, MOE_EINVAL, "hidden and inter must be multiples of 4 (f32) or 8 (bf16)");
+    return fail(nullptr, MOE_EINVAL, "hidden and inter must be multiples of 4 (f32), 8 (bf16) or 16 (fp8)");
   if (g.mlp_kernel != MOE_MLP_AUTO && g.mlp_kernel != MOE_MLP_PLAIN)
     return fail(nullptr, MOE_EINVAL, "mlp_kernel must be MOE_MLP_AUTO or MOE_MLP_PLAIN");
   if (g.copy_mode < MOE_COPY_AUTO || g.copy_mode > MOE_COPY_FUSED)

@@ -66,7 +66,7 @@ extern "C" moe_status moe_expert_mlp_noalloc(int wdtype, int hidden, int inter, 
                                              const void* x_d, const uint64_t* block_ptrs_d,
                                              const float* w_d, int T, void* y_d, int flags,
                                              moe_stream_t stream) {
-  if (wdtype != MOE_F32 && wdtype != MOE_BF16 && wdtype != MOE_INT4_G128)
+  if (wdtype != MOE_F32 && wdtype != MOE_BF16 && wdtype != MOE_INT4_G128 && wdtype != MOE_FP8_E4M3)
     return set_global_error(MOE_EINVAL, "moe_expert_mlp_noalloc: bad wdtype");
   if (hidden <= 0 || inter <= 0 || hidden % chunk_elems(wdtype) || inter % chunk_elems(wdtype) ||
       (wdtype == MOE_INT4_G128 && (hidden % 128 || inter % 128)))

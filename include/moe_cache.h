@@ -63,8 +63,15 @@ typedef void* moe_stream_t;             /* cudaStream_t */
  *                multiples of 128.  At w13 [1280, 2560] + w2 [2560, 640] this
  *                is 2,534,400 bytes = 2.417 MiB ([Flash-Next 2x32GB] section 1
  *                "What does not fit").
+ *  MOE_FP8_E4M3  one OCP E4M3 byte per weight (sign, 4 exponent bits with bias
+ *                7, 3 mantissa bits, exponent 0 = subnormal, no infinities,
+ *                S.1111.111 = NaN); per-tensor scales ([vLLM #37190] "BF16 +
+ *                FP8 per-tensor", scale buffers copied with the weights):
+ *                s13 = float32 [gate scale, up scale] and s2 = float32 [down
+ *                scale], each part zero-padded to 16 bytes; weight = decoded
+ *                byte * its tensor's scale.  H and I must be multiples of 16.
  * Hidden states x / y are f32 for MOE_F32 and bf16 otherwise. */
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_INT4_G128 = 2 } moe_wdtype;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_INT4_G128 = 2, MOE_FP8_E4M3 = 3 } moe_wdtype;
 
 /* How missed experts reach their slot.
  *  MOE_COPY_MEMCPY  prepare reads the miss list back to the host (one small

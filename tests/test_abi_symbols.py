@@ -55,5 +55,6 @@ def test_expert_bytes_without_gpu(built_lib):
     from expert_slot_cache_topk_gb300 import _abi
     assert _abi.expert_bytes("int4g128", 2560, 640) == 2_534_400
     assert _abi.expert_bytes("bf16", 2048, 1024) == 12 * 2 ** 20
+    assert _abi.expert_bytes("fp8", 2048, 1024) == 3 * 2048 * 1024 + 32
     with pytest.raises(_abi.MoeError):
         _abi.expert_bytes("int4g128", 2560, 100)
