@@ -372,7 +372,7 @@ def run_ours(args, w):
 
     S = args.warmup + args.steps
     c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, w.tokens,
-                 copy_mode=args.copy_mode, device=local_rank)
+                 copy_mode=args.copy_mode, device=local_rank, table=args.table)
     info = c.info()
     t0 = time.time()
     for l in range(w.layers):
@@ -458,6 +458,27 @@ def run_ours(args, w):
         launches = eager_launches
     st1 = c.stats(-1)
     del graph
+    # (1b) cold start: every step from an empty pool (warm-up steps included),
+    # replayed from a graph uploaded by one untimed replay
+    cold_sec = None
+    if use_graph:
+        c.reset()
+        gc = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gc, stream=stream):
+                for s in range(S):
+                    step(s, stream)
+            gc.replay()
+        stream.synchronize()
+        c.reset()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            gc.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        cold_sec = e0.elapsed_time(e1) / 1e3
+        del gc
     # (2) the same steps from the same state again, with per-launch events and
     # miss counts, for the kernel roofline and the per-miss fit
     graph_t, _ = prime(True)
@@ -508,7 +529,7 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.wdtype],
             "data": "synthetic (seeded Zipf routing with reuse; N(0,0.02) weights)",
             "config": {"workload": workload_desc(w), "tokens_per_step": w.tokens,
-                       "copy_mode": info["copy_mode_name"], "graph": use_graph,
+                       "copy_mode": info["copy_mode_name"], "graph": use_graph, "table": args.table,
                        "l2": "inputs larger than L2: every step reads "
                              f"{w.layers * w.top_k * lay['total'] / 1e9:.2f} GB of expert weights",
                        "parallelism": f"replicas x{world}"},
@@ -526,7 +547,11 @@ def run_ours(args, w):
                     "mlp_us_by_misses": {str(m): float(mlp_ms[(mlp_miss == m) & (mlp_ms > 0)].mean() * 1e3)
                                          for m in range(4) if ((mlp_miss == m) & (mlp_ms > 0)).any()}},
             "phases_ms_per_step": {k[:-3]: tm[k] / args.steps for k in ("route_ms", "copy_ms", "up_ms", "down_ms")},
-            "cache": {k: st1[k] - st0[k] for k in ("hits", "misses", "evictions", "bypass_steps")},
+            "cache": dict({k: st1[k] - st0[k] for k in ("hits", "misses", "evictions", "bypass_steps")},
+                          hit_rate=(st1["hits"] - st0["hits"]) / max(1, st1["hits"] - st0["hits"] + st1["misses"] - st0["misses"])),
+            "cold_start": ({"value": S * w.tokens / cold_sec, "unit": UNIT, "steps": S,
+                            "note": "all steps from an empty pool, warm-up steps included"}
+                           if cold_sec else None),
             "e2e": {"value": (e2e_tok / e2e_sec) if e2e_steps > 0 else None, "unit": UNIT,
                     "h2d_bytes_per_step": int(x_h[0].nbytes + lg_h[0].nbytes),
                     "d2h_bytes_per_step": int(y_h.nbytes)},
@@ -560,6 +585,8 @@ def main():
     ap.add_argument("--copy-mode", default="auto", choices=["auto", "uva", "memcpy", "fused"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling case)")
     ap.add_argument("--slots", type=int, default=-1, help="override the pool slots per layer (N)")
+    ap.add_argument("--table", default="split", choices=["split", "vmm"],
+                    help="pool + backing store as two allocations, or one VMM table per layer")
     ap.add_argument("--wdtype", default="", choices=["", "f32", "bf16", "int4g128", "fp8"],
                     help="override the decode workload's weight format")
     ap.add_argument("--clock-ms", type=int, default=100, help="nvidia-smi sampling interval in ms")

@@ -27,6 +27,8 @@ MOE_MLP_AUTO, MOE_MLP_PLAIN = 0, 1
 MLP_KERNEL = {"auto": MOE_MLP_AUTO, "plain": MOE_MLP_PLAIN}
 MOE_EVICT_LRU, MOE_EVICT_LFU, MOE_EVICT_FIFO, MOE_EVICT_SLRU = 0, 1, 2, 3
 EVICT_POLICY = {"lru": MOE_EVICT_LRU, "lfu": MOE_EVICT_LFU, "fifo": MOE_EVICT_FIFO, "slru": MOE_EVICT_SLRU}
+MOE_TABLE_SPLIT, MOE_TABLE_VMM = 0, 1
+TABLE_LAYOUT = {"split": MOE_TABLE_SPLIT, "vmm": MOE_TABLE_VMM}
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ETIMEOUT, MOE_ESTATE = 0, -1, -2, -3, -4, -5
 STATUS_NAME = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ENOMEM", -3: "MOE_ECUDA",
                -4: "MOE_ETIMEOUT", -5: "MOE_ESTATE"}
@@ -42,7 +44,7 @@ class moe_cache_config(C.Structure):
                 ("cold_mask_h", C.POINTER(C.c_uint8)), ("copy_mode", C.c_int), ("device", C.c_int),
                 ("hbm_budget_bytes", C.c_size_t), ("mlp_kernel", C.c_int),
                 ("move_interval", C.c_int), ("move_decay", C.c_float), ("move_threshold", C.c_float),
-                ("move_count_tokens", C.c_int), ("evict_policy", C.c_int)]
+                ("move_count_tokens", C.c_int), ("evict_policy", C.c_int), ("table_layout", C.c_int)]
 
 
 class moe_cache_counters(C.Structure):
@@ -65,7 +67,7 @@ class moe_cache_info(C.Structure):
                 ("pool_bytes", C.c_size_t), ("scratch_bytes", C.c_size_t),
                 ("backing_bytes", C.c_size_t), ("copy_mode", C.c_int), ("memcpy_gbs", C.c_double),
                 ("uva_gbs", C.c_double), ("kernel_launches", C.c_uint64),
-                ("scratch_experts", C.c_int)]
+                ("scratch_experts", C.c_int), ("table_layout", C.c_int)]
 
 
 class moe_cache_timing(C.Structure):
@@ -185,10 +187,11 @@ class MoECache:
 
     def __init__(self, num_layers, num_experts, top_k, hidden, inter, wdtype, slots, max_tokens,
                  renormalize=False, cold_mask=None, copy_mode="uva", device=0, hbm_budget_bytes=0,
-                 mlp_kernel="auto", moves=None, policy="lru"):
+                 mlp_kernel="auto", moves=None, policy="lru", table="split"):
         """moves: None (off) or a dict with interval, decay, threshold, count_tokens
         (run-time moves between the cold set and the pool; see moe_cache_config).
-        policy: the eviction policy, one of EVICT_POLICY's keys."""
+        policy: the eviction policy, one of EVICT_POLICY's keys.
+        table: "split" (device pool + pinned backing store) or "vmm" (one VMM table per layer)."""
         self.L, self.E, self.k, self.H, self.I = num_layers, num_experts, top_k, hidden, inter
         self.wdtype, self.N, self.max_tokens = wdtype, slots, max_tokens
         cfg = moe_cache_config()
@@ -206,6 +209,7 @@ class MoECache:
         cfg.hbm_budget_bytes = hbm_budget_bytes
         cfg.mlp_kernel = MLP_KERNEL[mlp_kernel]
         cfg.evict_policy = EVICT_POLICY[policy]
+        cfg.table_layout = TABLE_LAYOUT[table]
         if moves:
             cfg.move_interval = int(moves.get("interval", 8))
             cfg.move_decay = float(moves.get("decay", 2.0 ** (-1.0 / 64.0)))

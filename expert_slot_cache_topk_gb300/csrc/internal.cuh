@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+#include <vector>
+
 #include "moe_cache.h"
 
 namespace moe {
@@ -164,6 +167,21 @@ cudaError_t mlp_ring_configure(int wdtype, int H, int I, int k);  // call outsid
 cudaError_t launch_mlp_ring(int wdtype, const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s);
 // floats the staged kernel's h scratch needs (it keeps several copies of h)
 size_t mlp_ring_h_floats(int k, int I);
+
+// ---- one VMM table per layer: device rows (pool), then host rows (backing store) (table_vmm.cu)
+struct VmmTable {
+  unsigned long long va = 0;       // CUdeviceptr of the reserved range
+  size_t bytes = 0;                // layers * pitch
+  size_t pitch = 0;                // bytes per layer: pool_part + host_part
+  size_t pool_part = 0, host_part = 0;
+  // per layer: allocation handles (CUmemGenericAllocationHandle, 0 = none) and
+  // whether each part is mapped (cuMemMap maps whole allocations only)
+  std::vector<unsigned long long> hdev, hhost;
+  std::vector<char> dev_mapped, host_mapped;
+};
+bool vmm_table_create(int device, int host_numa, int layers, size_t pool_bytes, size_t host_bytes, VmmTable* t,
+                      std::string* err);
+void vmm_table_destroy(VmmTable* t);
 
 // ---- launchers (k_moe_gemm.cu): grouped expert MLP on the tensor cores for
 // steps with several tokens (group by expert, tcgen05 up and down GEMMs,

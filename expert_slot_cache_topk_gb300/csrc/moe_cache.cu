@@ -67,8 +67,11 @@ struct moe_cache {
   int L = 0, E = 0, K = 0, H = 0, I = 0, N = 0, maxT = 0, wd = 0;
   size_t Be = 0, stride = 0, nvec = 0, off_w2 = 0, off_s13 = 0, off_s2 = 0;
   int scratch_n = 0;
-  uint8_t* backing_h = nullptr;   // pinned, device-mapped
+  uint8_t* backing_h = nullptr;   // pinned, device-mapped (or the host rows of the VMM table)
   uint8_t* backing_dv = nullptr;  // its device-usable address
+  size_t pool_pitch = 0;          // bytes from one layer's pool to the next
+  size_t back_pitch = 0;          // bytes from one layer's backing store to the next
+  VmmTable vmm;                   // MOE_TABLE_VMM: the reserved table of all layers
   bool staged_mlp = false;        // one-token steps may use the staged-weight kernel
   bool gemm_mlp = false;          // multi-token steps may use the tensor-core grouped GEMM
   int32_t* order_d = nullptr;     // grouped GEMM: assignments grouped by expert
@@ -123,6 +126,11 @@ struct moe_cache {
 };
 
 namespace {
+
+// layer l's pool slots, and its backing store as the host and the device see it
+uint8_t* pool_of(const moe_cache* c, int l) { return c->pool_d + (size_t)l * c->pool_pitch; }
+uint8_t* back_h_of(const moe_cache* c, int l) { return c->backing_h + (size_t)l * c->back_pitch; }
+uint8_t* back_d_of(const moe_cache* c, int l) { return c->backing_dv + (size_t)l * c->back_pitch; }
 
 moe_status fail(moe_cache* c, moe_status st, const std::string& msg) {
   if (c) c->err = msg;
@@ -245,9 +253,9 @@ moe_status run_prepare(moe_cache* c, int layer, const float* logits, const int32
   a.asg_ptr = c->asg_d;
   a.src_ptr = c->src_d;
   a.pending = c->pend_d;
-  a.pool_base = (unsigned long long)(c->pool_d + (size_t)layer * c->N * c->stride);
+  a.pool_base = (unsigned long long)pool_of(c, layer);
   a.scratch_base = (unsigned long long)c->scratch_d;
-  a.host_base = (unsigned long long)(c->backing_dv + (size_t)layer * c->E * c->stride);
+  a.host_base = (unsigned long long)back_d_of(c, layer);
   a.stride = c->stride;
   a.expert_bytes = c->Be;
   a.err = c->err_d;
@@ -317,7 +325,7 @@ cudaError_t launch_layer_mlp(moe_cache* c, const MlpArgs& m, cudaStream_t s, int
 // overlap was measured slower; the kernels keep the pass filter for callers
 // that want it.)  `mlp` null = prepare only.
 moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const MlpArgs* mlp) {
-  uint8_t* pool = c->pool_d + (size_t)layer * c->N * c->stride;
+  uint8_t* pool = pool_of(c, layer);
   if (c->copy_mode == MOE_COPY_FUSED && mlp != nullptr && mlp->T == 1) {
     // read-through: the fused expert-MLP kernel fills the slots itself
     MlpArgs m = *mlp;
@@ -357,7 +365,7 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
     a.hdr = c->hdr_d + layer;
     a.lists = c->lists_d + (size_t)layer * LST_COUNT * c->E;
     a.E = c->E;
-    a.host_base = c->backing_dv + (size_t)layer * c->E * c->stride;
+    a.host_base = back_d_of(c, layer);
     a.pool_base = pool;
     a.scratch_base = c->scratch_d;
     a.stride = c->stride;
@@ -409,7 +417,7 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
     a.hdr = c->hdr_d + layer;
     a.lists = c->lists_d + (size_t)layer * LST_COUNT * c->E;
     a.E = c->E;
-    a.host_base = c->backing_dv + (size_t)layer * c->E * c->stride;
+    a.host_base = back_d_of(c, layer);
     a.pool_base = pool;
     a.scratch_base = c->scratch_d;
     a.stride = c->stride;
@@ -431,10 +439,10 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
       const int ti = tm_begin(c, TM_COPY, c->copy_stream);
       const int32_t* src = c->lists_h + (h.bypass ? LST_NONCOLD : LST_MISS_E) * c->E;
       const int32_t* slot = c->lists_h + LST_MISS_SLOT * c->E;
-      const uint8_t* host = c->backing_h + (size_t)layer * c->E * c->stride;
+      const uint8_t* host = back_h_of(c, layer);
       for (int i = 0; i < n; ++i) {
         uint8_t* dst = h.bypass ? c->scratch_d + (size_t)i * c->stride : pool + (size_t)slot[i] * c->stride;
-        CK(c, cudaMemcpyAsync(dst, host + (size_t)src[i] * c->stride, c->Be, cudaMemcpyHostToDevice,
+        CK(c, cudaMemcpyAsync(dst, host + (size_t)src[i] * c->stride, c->Be, cudaMemcpyDefault,
                               c->copy_stream));
       }
       tm_end(c, TM_COPY, ti, c->copy_stream);
@@ -491,13 +499,14 @@ MlpArgs mlp_args(int wd, int H, int I, int k, const void* x, const unsigned long
 
 moe_status measure_copy_modes(moe_cache* c) {
   // Time a pinned-host -> HBM copy both ways on the handle's own buffers.
-  size_t dev_bytes = (size_t)c->L * c->N * c->stride;
+  // (layer 0's pool or the scratch, from layer 0's backing store: contiguous in either table layout)
+  size_t dev_bytes = (size_t)c->N * c->stride;
   uint8_t* dst = c->pool_d;
   if (dev_bytes < (size_t)c->scratch_n * c->stride) {
     dev_bytes = (size_t)c->scratch_n * c->stride;
     dst = c->scratch_d;
   }
-  size_t bytes = std::min(std::min(dev_bytes, (size_t)c->L * c->E * c->stride), (size_t)256 << 20);
+  size_t bytes = std::min(std::min(dev_bytes, (size_t)c->E * c->stride), (size_t)256 << 20);
   bytes &= ~(size_t)15;
   if (bytes == 0) return MOE_OK;
   cudaStream_t s = c->copy_stream;
@@ -507,7 +516,7 @@ moe_status measure_copy_modes(moe_cache* c) {
   float best_m = 1e30f, best_u = 1e30f, ms = 0;
   for (int rep = 0; rep < 3; ++rep) {
     CK(c, cudaEventRecord(a, s));
-    CK(c, cudaMemcpyAsync(dst, c->backing_h, bytes, cudaMemcpyHostToDevice, s));
+    CK(c, cudaMemcpyAsync(dst, c->backing_h, bytes, cudaMemcpyDefault, s));
     CK(c, cudaEventRecord(b, s));
     CK(c, cudaEventSynchronize(b));
     CK(c, cudaEventElapsedTime(&ms, a, b));
@@ -541,6 +550,11 @@ void free_all(moe_cache* c) {
   if (c->ev_join) cudaEventDestroy(c->ev_join);
   if (c->ev_sync) cudaEventDestroy(c->ev_sync);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+  if (c->vmm.va) {
+    vmm_table_destroy(&c->vmm);
+    c->pool_d = nullptr;
+    c->backing_h = nullptr;
+  }
   void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->fstack_d, c->counts_d, c->slot_map_d, c->slot_expert_d,
                  c->slot_stamp_d, c->slot_aux_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
                  c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->ring_cnt_d, c->tm_miss_d, c->xs_d[0], c->xs_d[1],
@@ -629,6 +643,8 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   if (g.copy_mode < MOE_COPY_AUTO || g.copy_mode > MOE_COPY_FUSED)
     return fail(nullptr, MOE_EINVAL, "bad copy_mode");
   if (g.renormalize != 0 && g.renormalize != 1) return fail(nullptr, MOE_EINVAL, "renormalize must be 0 or 1");
+  if (g.table_layout != MOE_TABLE_SPLIT && g.table_layout != MOE_TABLE_VMM)
+    return fail(nullptr, MOE_EINVAL, "table_layout must be MOE_TABLE_SPLIT or MOE_TABLE_VMM");
   if (g.evict_policy < MOE_EVICT_LRU || g.evict_policy > MOE_EVICT_SLRU)
     return fail(nullptr, MOE_EINVAL, "evict_policy must be MOE_EVICT_LRU, _LFU, _FIFO or _SLRU");
   if (g.move_interval < 0) return fail(nullptr, MOE_EINVAL, "move_interval must be >= 0");
@@ -694,16 +710,35 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
     return bail(MOE_ENOMEM);
   }
   const size_t backing_bytes = (size_t)c->L * c->E * c->stride;
-  if (cudaHostAlloc((void**)&c->backing_h, backing_bytes, cudaHostAllocMapped | cudaHostAllocPortable) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    c->backing_h = nullptr;
-    fail(c, MOE_ENOMEM, "cudaHostAlloc of the pinned backing store failed");
-    return bail(MOE_ENOMEM);
-  }
-  CKC(cudaHostGetDevicePointer((void**)&c->backing_dv, c->backing_h, 0));
   auto dmalloc = [&](void** p, size_t n) { return cudaMalloc(p, n ? n : 16); };
-  if (dmalloc((void**)&c->pool_d, pool_bytes) != cudaSuccess ||
+  if (g.table_layout == MOE_TABLE_VMM) {
+    int numa = -1;
+    if (cudaDeviceGetAttribute(&numa, cudaDevAttrHostNumaId, g.device) != cudaSuccess) {
+      cudaGetLastError();
+      numa = 0;
+    }
+    std::string why;
+    if (!vmm_table_create(g.device, numa, c->L, (size_t)c->N * c->stride, (size_t)c->E * c->stride, &c->vmm,
+                          &why)) {
+      fail(c, MOE_ECUDA, "one VMM table per layer: " + why);
+      return bail(MOE_ECUDA);
+    }
+    c->pool_d = reinterpret_cast<uint8_t*>(c->vmm.va);
+    c->backing_h = c->backing_dv = reinterpret_cast<uint8_t*>(c->vmm.va + c->vmm.pool_part);
+    c->pool_pitch = c->back_pitch = c->vmm.pitch;
+  } else {
+    if (cudaHostAlloc((void**)&c->backing_h, backing_bytes, cudaHostAllocMapped | cudaHostAllocPortable) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      c->backing_h = nullptr;
+      fail(c, MOE_ENOMEM, "cudaHostAlloc of the pinned backing store failed");
+      return bail(MOE_ENOMEM);
+    }
+    CKC(cudaHostGetDevicePointer((void**)&c->backing_dv, c->backing_h, 0));
+    c->pool_pitch = (size_t)c->N * c->stride;
+    c->back_pitch = (size_t)c->E * c->stride;
+  }
+  if ((g.table_layout != MOE_TABLE_VMM && dmalloc((void**)&c->pool_d, pool_bytes) != cudaSuccess) ||
       dmalloc((void**)&c->scratch_d, scratch_bytes) != cudaSuccess) {
     cudaGetLastError();
     fail(c, MOE_ENOMEM, "cudaMalloc of the slot pools failed");
@@ -793,6 +828,7 @@ moe_status moe_cache_get_info(moe_cache_t* c, moe_cache_info* out) {
   out->uva_gbs = c->uva_gbs;
   out->kernel_launches = c->launches;
   out->scratch_experts = c->scratch_n;
+  out->table_layout = c->cfg.table_layout;
   return MOE_OK;
 }
 
@@ -801,7 +837,7 @@ moe_status moe_cache_backing_ptr(moe_cache_t* c, int layer, int expert, void** b
   moe_status st = check_layer(c, layer);
   if (st != MOE_OK) return st;
   if (expert < 0 || expert >= c->E || !block_h) return fail(c, MOE_EINVAL, "expert out of range or null out");
-  *block_h = c->backing_h + ((size_t)layer * c->E + expert) * c->stride;
+  *block_h = back_h_of(c, layer) + (size_t)expert * c->stride;
   if (stride_bytes) *stride_bytes = c->stride;
   return MOE_OK;
 }
@@ -814,12 +850,12 @@ moe_status moe_cache_load_expert(moe_cache_t* c, int layer, int expert, const vo
     return fail(c, MOE_EINVAL, "expert out of range, null block or wrong byte count");
   CK(c, cudaSetDevice(c->cfg.device));
   CK(c, cudaDeviceSynchronize());
-  uint8_t* dst = c->backing_h + ((size_t)layer * c->E + expert) * c->stride;
+  uint8_t* dst = back_h_of(c, layer) + (size_t)expert * c->stride;
   memcpy(dst, block_h, bytes);
   int32_t s = -1;
   CK(c, cudaMemcpy(&s, c->slot_map_d + (size_t)layer * c->E + expert, sizeof s, cudaMemcpyDeviceToHost));
   if (s >= 0)
-    CK(c, cudaMemcpy(c->pool_d + ((size_t)layer * c->N + s) * c->stride, dst, bytes, cudaMemcpyHostToDevice));
+    CK(c, cudaMemcpy(pool_of(c, layer) + (size_t)s * c->stride, dst, bytes, cudaMemcpyDefault));
   return MOE_OK;
 }
 
@@ -894,8 +930,9 @@ moe_status moe_forward(moe_cache_t* c, int layer, const void* x_d, const float* 
   st = run_prepare(c, layer, logits_d, nullptr, T, nullptr, s);
   if (st != MOE_OK) return st;
   MlpArgs a = mlp_args(c->wd, c->H, c->I, c->K, x_d, c->asg_d, c->w_d, c->h_d, y_d, T, flags);
-  a.host_lo = (unsigned long long)c->backing_dv;
-  a.host_hi = a.host_lo + (unsigned long long)c->L * c->E * c->stride;
+  // this layer's host rows (in the VMM layout they sit between two layers' pools)
+  a.host_lo = (unsigned long long)back_d_of(c, layer);
+  a.host_hi = a.host_lo + (unsigned long long)c->E * c->stride;
   return run_copies_and_mlp(c, layer, s, &a);
 }
 
@@ -1055,8 +1092,7 @@ moe_status moe_cache_verify_slots(moe_cache_t* c, int layer, int* mismatched_slo
   CK(c, cudaDeviceSynchronize());
   CK(c, cudaMemset(c->verify_d, 0, sizeof(int)));
   CK(c, launch_verify(c->slot_expert_d + (size_t)layer * c->N, c->N,
-                      c->pool_d + (size_t)layer * c->N * c->stride,
-                      c->backing_dv + (size_t)layer * c->E * c->stride, c->stride, c->nvec,
+                      pool_of(c, layer), back_d_of(c, layer), c->stride, c->nvec,
                       c->verify_d, 0));
   c->launches++;
   CK(c, cudaDeviceSynchronize());
@@ -1077,7 +1113,7 @@ moe_status moe_cache_get_cold(moe_cache_t* c, int layer, uint8_t* cold_h) {
 moe_status moe_cache_pool_ptrs(moe_cache_t* c, int layer, void** pool_d, void** scratch_d) {
   moe_status st = check_layer(c, layer);
   if (st != MOE_OK) return st;
-  if (pool_d) *pool_d = c->pool_d + (size_t)layer * c->N * c->stride;
+  if (pool_d) *pool_d = pool_of(c, layer);
   if (scratch_d) *scratch_d = c->scratch_d;
   return MOE_OK;
 }

@@ -122,6 +122,20 @@ typedef enum { MOE_MLP_AUTO = 0, MOE_MLP_PLAIN = 1 } moe_mlp_kernel;
  *         else the protected least recent one. */
 typedef enum { MOE_EVICT_LRU = 0, MOE_EVICT_LFU = 1, MOE_EVICT_FIFO = 2, MOE_EVICT_SLRU = 3 } moe_evict_policy;
 
+/* Where the pool slots and the backing store live.
+ *  MOE_TABLE_SPLIT  slots in device memory (cudaMalloc), backing store in pinned,
+ *                   device-mapped host memory (cudaHostAlloc): two allocations.
+ *  MOE_TABLE_VMM    one virtual-address table per layer ([Flash-Next 2x32GB]
+ *                   section 4.2): cuMemAddressReserve, cuMemCreate of device rows
+ *                   and of host rows on the device's host NUMA node, cuMemMap of
+ *                   the two side by side, so row r < N of layer l's table is pool
+ *                   slot r and row N + e is expert e's backing copy (each part
+ *                   rounded up to the allocation granularity).  The CPU writes the
+ *                   backing store through the same addresses.  moe_cache_create
+ *                   fails with MOE_ECUDA (message from the driver) if the driver
+ *                   refuses any step; nothing falls back silently. */
+typedef enum { MOE_TABLE_SPLIT = 0, MOE_TABLE_VMM = 1 } moe_table_layout;
+
 typedef enum {
   MOE_OK = 0,
   MOE_EINVAL = -1,    /* bad argument, nothing done */
@@ -180,6 +194,7 @@ typedef struct {
   float move_threshold;  /* >= 0 */
   int move_count_tokens; /* >= 1 */
   int evict_policy;      /* moe_evict_policy */
+  int table_layout;      /* moe_table_layout */
 } moe_cache_config;
 
 /* Cumulative per-layer counters (moe_cache_stats with layer = -1 sums layers).
@@ -225,6 +240,7 @@ typedef struct {
   double uva_gbs;            /* measured at create (AUTO only, else 0) */
   uint64_t kernel_launches;  /* kernels launched by this handle so far */
   int scratch_experts;       /* bypass scratch capacity in experts */
+  int table_layout;          /* moe_table_layout in use */
 } moe_cache_info;
 
 /* Per-phase GPU time accumulated while timing is on (CUDA events on the
