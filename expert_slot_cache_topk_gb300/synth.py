@@ -107,9 +107,7 @@ def expert_layout(wdtype: str, hidden: int, inter: int) -> dict:
     """Byte offsets of one expert block: [w13 | w2 | s13 | s2].
 
     w13 is [2*inter, hidden] (rows [0, inter) gate, [inter, 2*inter) up),
-    row-major; w2 is [hidden, inter], row-major for INT4 and FP8 and, for f32
-    and bf16, in column panels [inter/EL][hidden][EL] of one 16-byte chunk
-    (EL = 4 or 8).  INT4: two weights per byte along
+    w2 is [hidden, inter], both row-major.  INT4: two weights per byte along
     the row, low nibble = even column; s13 [2*inter, hidden/128] and
     s2 [hidden, inter/128] bf16 scales.  FP8: one E4M3 byte per weight;
     s13 = float32 [gate scale, up scale] and s2 = float32 [down scale], each
@@ -187,12 +185,6 @@ def _quantize_int4_g128(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return packed, s_bits
 
 
-def _to_panels(m: np.ndarray, EL: int) -> np.ndarray:
-    """[H, I] -> column panels [I / EL][H][EL], flattened."""
-    H, I = m.shape
-    return np.ascontiguousarray(m.reshape(H, I // EL, EL).transpose(1, 0, 2)).reshape(-1)
-
-
 _E4M3_POS = None
 
 
@@ -236,13 +228,12 @@ def expert_block(w: Workload, layer: int, expert: int, out: Optional[np.ndarray]
         o, n = lay["w13"]
         out[o:o + n] = _normal_f32(g, 2 * I * H, WEIGHT_STD).view(np.uint8)
         o, n = lay["w2"]
-        out[o:o + n] = _to_panels(_normal_f32(g, H * I, WEIGHT_STD).reshape(H, I), 4).view(np.uint8)
+        out[o:o + n] = _normal_f32(g, H * I, WEIGHT_STD).view(np.uint8)
     elif w.wdtype == "bf16":
         o, n = lay["w13"]
         out[o:o + n] = _f32_to_bf16_bits(_normal_f32(g, 2 * I * H, WEIGHT_STD)).view(np.uint8)
         o, n = lay["w2"]
-        w2 = _f32_to_bf16_bits(_normal_f32(g, H * I, WEIGHT_STD)).reshape(H, I)
-        out[o:o + n] = _to_panels(w2, 8).view(np.uint8)
+        out[o:o + n] = _f32_to_bf16_bits(_normal_f32(g, H * I, WEIGHT_STD)).view(np.uint8)
     elif w.wdtype == "fp8":
         w13 = _normal_f32(g, 2 * I * H, WEIGHT_STD).reshape(2 * I, H)
         qg, sg = _quantize_fp8(w13[:I])

@@ -28,13 +28,7 @@ Readings where the pages are open
   down (w2).  s13 = [gate scale, up scale] and s2 = [down scale], each part
   zero-padded to 16 bytes.
 
-Canonical block layout: [w13 | w2 | s13 | s2].  w13 [2I, H] is row-major in
-every format; so are the INT4 and FP8 w2 [H, I].  f32 and bf16 store w2 in
-column panels of one 16-byte chunk: panel c (columns [c * EL, (c + 1) * EL),
-EL = 4 for f32, 8 for bf16) holds, row after row, those EL weights of all H
-rows, so element (n, i) sits at ((i // EL) * H + n) * EL + i % EL.  (The
-pages fix the parts' sizes, not their order in memory: a decode step reads
-one panel for every group of EL intermediate columns it computes.)
+Canonical block layout: [w13 | w2 | s13 | s2], each part row-major.
 """
 
 from __future__ import annotations
@@ -87,12 +81,6 @@ def dequant_int4_g128(packed: np.ndarray, scale_bits: np.ndarray, rows: int, K: 
     return (q - 8).astype(np.float64) * s[:, col_group]
 
 
-def panels_to_rows(vals: np.ndarray, H: int, I: int, EL: int) -> np.ndarray:
-    """w2 values stored as column panels [I / EL][H][EL] -> the matrix [H, I]."""
-    p = np.asarray(vals).reshape(I // EL, H, EL)
-    return p.transpose(1, 0, 2).reshape(H, I)
-
-
 def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
     """OCP E4M3 bytes -> float64, from the format's definition (exact)."""
     c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
@@ -115,10 +103,10 @@ def dequant_expert(block: np.ndarray, wdtype: str, H: int, I: int):
     parts = split_block(block, wdtype, H, I)
     if wdtype == "f32":
         w13 = parts["w13"].view(np.float32).astype(np.float64).reshape(2 * I, H)
-        w2 = panels_to_rows(parts["w2"].view(np.float32).astype(np.float64), H, I, 4)
+        w2 = parts["w2"].view(np.float32).astype(np.float64).reshape(H, I)
     elif wdtype == "bf16":
         w13 = bf16_bits_to_f64(parts["w13"].view(np.uint16)).reshape(2 * I, H)
-        w2 = panels_to_rows(bf16_bits_to_f64(parts["w2"].view(np.uint16)), H, I, 8)
+        w2 = bf16_bits_to_f64(parts["w2"].view(np.uint16)).reshape(H, I)
     elif wdtype == "fp8":
         s13 = parts["s13"].view(np.float32)
         s2 = parts["s2"].view(np.float32)

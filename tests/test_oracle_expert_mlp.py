@@ -205,32 +205,3 @@ def test_planted_mistakes_are_caught(monkeypatch):
     H = I = 4
     y = M.swiglu_expert(np.ones(H), np.concatenate([np.eye(I), np.eye(I)]), np.eye(H))
     assert abs(y[0] - 1.0 / (1 + math.exp(-1.0))) > 0.1
-
-
-# ---------------------------------------------------------------------------
-# w2 column panels (f32 / bf16)
-# ---------------------------------------------------------------------------
-
-@pytest.mark.parametrize("wdtype,EL,nbytes", [("f32", 4, 4), ("bf16", 8, 2)])
-def test_w2_panel_layout_by_hand(wdtype, EL, nbytes):
-    """Place w2[n, i] = n * I + i (integers below 256: exact in bf16) byte by
-    byte at ((i // EL) * H + n) * EL + i % EL, element by element, and read it
-    back."""
-    H, I = 8, 32
-    n = expert_nbytes(wdtype, H, I)
-    blk = np.zeros(n["total"], np.uint8)
-    want = np.zeros((H, I))
-    for r in range(H):
-        for i in range(I):
-            v = float(r * I + i)
-            want[r, i] = v
-            pos = ((i // EL) * H + r) * EL + i % EL
-            raw = np.float32(v).tobytes() if wdtype == "f32" else (np.float32(v).view(np.uint32) >> 16).astype("<u2").tobytes()
-            o = n["w13"] + pos * nbytes
-            blk[o:o + nbytes] = np.frombuffer(raw, np.uint8)
-    _, w2 = dequant_expert(blk, wdtype, H, I)
-    assert np.array_equal(w2, want)
-    # planted mistake: the w2 bytes read as a row-major [H, I] matrix
-    raw = blk[n["w13"]: n["w13"] + n["w2"]]
-    vals = raw.view(np.float32) if wdtype == "f32" else bf16_bits_to_f64(raw.view(np.uint16))
-    assert not np.array_equal(np.asarray(vals, np.float64).reshape(H, I), want)
