@@ -296,7 +296,7 @@ def run_prefill(args, dev, world):
     T = w.prefill_tokens
     cold = np.stack([synth.cold_mask(w, l) for l in range(w.layers)])
     c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, T,
-                 cold_mask=cold, copy_mode="uva", device=dev.index)
+                 cold_mask=cold, copy_mode="auto", device=dev.index)
     info = c.info()
     for l in range(w.layers):
         synth.fill_layer_blocks(w, l, c.backing_view(l).reshape(-1), info["slot_stride"])
@@ -330,6 +330,7 @@ def run_prefill(args, dev, world):
     tm = c.read_timing()
     c.set_timing(False)
     st1 = c.stats(-1)
+    dec = decode_after_prefill(c, w, dev, stream, world)
     c.close()
     max_sec, all_tok = aggregate(sec, reps * T, world, dev)
     lay = synth.expert_layout(w.wdtype, w.hidden, w.inter)
@@ -354,7 +355,61 @@ def run_prefill(args, dev, world):
         "bypass_copy": {"bytes_per_chunk": byp // reps, "ms_per_chunk": 1e3 * copy_s / reps,
                         "gbs": byp / copy_s / 1e9 if copy_s > 0 else None},
         "cold_reads_per_chunk": (st1["cold_reads"] - st0["cold_reads"]) // reps,
+        "decode_after_prefill": dec,
     }
+
+
+def decode_after_prefill(c, w, dev, stream, world, warmup=32, steps=128):
+    """Decode steps of the same workload on the same cache after its prefill
+    chunks (batch 1, N slots, the cold set read in place): warm-up steps, then
+    the timed steps replayed from an uploaded graph from the warmed state."""
+    import torch
+    from expert_slot_cache_topk_gb300._abi import MOE_FWD_RESIDUAL
+    S = warmup + steps
+    lg = torch.from_numpy(np.stack([synth.routing_logits(w.with_(tokens=1), l, S) for l in range(w.layers)], 1)).to(dev)
+    x0 = torch.from_numpy(synth.hidden_states(w, 0, S, tokens=1).view(np.int16)).to(dev).view(torch.bfloat16)
+    ys = torch.empty((S, w.layers, 1, w.hidden), dtype=torch.bfloat16, device=dev)
+
+    def step(s):
+        x = x0[s]
+        for l in range(w.layers):
+            c.forward(l, x, lg[s, l], 1, ys[s, l], MOE_FWD_RESIDUAL, stream)
+            x = ys[s, l]
+
+    with torch.cuda.stream(stream):
+        for s in range(warmup):
+            step(s)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(warmup, S):
+                step(s)
+    stream.synchronize()
+    st_w = c.stats(-1)
+    with torch.cuda.stream(stream):
+        g.replay()                     # uploads the graph; the state moves on by `steps`
+    stream.synchronize()
+    st0 = c.stats(-1)
+    # replaying from the state after the first replay: the same steps again,
+    # the pool as those steps left it (the routing is stationary)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = ev0.elapsed_time(ev1) / 1e3
+    st1 = c.stats(-1)
+    del g
+    max_sec, all_tok = aggregate(sec, steps, world, dev)
+    hits, misses = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
+    return {"value": all_tok / max_sec, "unit": "tok/s", "steps": steps, "warmup_steps": warmup,
+            "copy_mode": c.info()["copy_mode_name"],
+            "misses_per_token": misses / steps, "cold_reads_per_token": (st1["cold_reads"] - st0["cold_reads"]) / steps,
+            "hit_rate": hits / max(1, hits + misses), "warm_misses": st0["misses"] - st_w["misses"]}
 
 
 def run_ours(args, w):
