@@ -758,10 +758,12 @@ __device__ __forceinline__ void produce(const MlpArgs& a, const RingCfg& rc, Rin
       __syncwarp();
       if (lane < a.k && !plain) {
         const uint8_t* blk = reinterpret_cast<const uint8_t*>(myb);
-        bulk_copy(smem_u32(st + (size_t)lane * wb), blk + a.off_w2 + (size_t)n * rb2, wb, full);
+        // W2 rows are read once per launch too: evict-first, so that they do
+        // not push the slot state and the prepare code out of L2
+        bulk_copy_hint(smem_u32(st + (size_t)lane * wb), blk + a.off_w2 + (size_t)n * rb2, wb, full, pol_first);
         if (sb != 0u)
-          bulk_copy(smem_u32(st + (size_t)a.k * wb + (size_t)lane * sb), blk + a.off_s2 + (size_t)n * srb2, sb,
-                    full);
+          bulk_copy_hint(smem_u32(st + (size_t)a.k * wb + (size_t)lane * sb), blk + a.off_s2 + (size_t)n * srb2, sb,
+                         full, pol_first);
       }
     }
   }
