@@ -81,14 +81,17 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_INT4_G128 = 2, MOE_FP8_E4M3 = 3 } 
  *  MOE_COPY_UVA     an SM copy kernel on the copy stream reads the device-side
  *                   miss list and copies from the mapped pinned host store with
  *                   16-byte loads.  No host round trip; graph-capturable.
- *  MOE_COPY_FUSED   single-token steps (decode): no separate copy.  The
- *                   expert-MLP kernel reads a missed expert's gate/up rows
- *                   straight from the pinned host store (the host link on
- *                   GB300 is coherent NVLink-C2C), computes with them and
- *                   writes them into the victim slot in the same pass; spare
- *                   warps copy the expert's w2 and scales into the slot at the
- *                   same time, so host-link traffic overlaps HBM streaming.
- *                   Steps with T > 1, and moe_cache_prepare, use the UVA copy
+ *  MOE_COPY_FUSED   single-token steps (decode): no separate copy launch.  A
+ *                   copier warp in every CTA of the expert-MLP kernel moves the
+ *                   missed experts' blocks from the pinned host store into
+ *                   their slots (the host link on GB300 is coherent
+ *                   NVLink-C2C) while the other warps compute with the experts
+ *                   already in HBM; a missed expert's rows are used once they
+ *                   have landed, so host-link traffic overlaps HBM streaming.
+ *                   When the staged kernel cannot take the shape, the
+ *                   cooperative kernel reads missed rows through instead.
+ *                   Steps with T > 1 use the flagged copy kernel overlapped
+ *                   with the grouped GEMM; moe_cache_prepare uses the UVA copy
  *                   kernel.  Graph-capturable.
  *  MOE_COPY_AUTO    at create, time cudaMemcpyAsync and the SM copy kernel on
  *                   the backing store; MEMCPY if it is more than 15% faster,
