@@ -944,7 +944,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_mlp_ring(MlpArgs a, RingCfg
   __shared__ RingShared S;
   // the next kernel of the stream (a prepare launched as a programmatic
   // dependent) may be scheduled now: it waits for this grid to complete
-  // before it touches memory, and its CTA fits beside this one
+  // before it touches memory.  Its CTA takes an SM as soon as one of this
+  // grid's CTAs exits (beside one it would need more than the SM's registers).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < a.k) {
