@@ -26,8 +26,8 @@
 // Kernel shape: persistent CTAs of 8 warps, work item = (tile of <= 128
 // assignments of one expert, N tile of 128 output columns).  For each K step
 // of 64 the threads stage A (gathered activation rows) and B (weight rows) in
-// shared memory as 8 x 16-byte core matrices with cp.async, two K steps ahead
-// of the MMAs over four stages; one thread issues four tcgen05.mma (K = 16
+// shared memory as 8 x 16-byte core matrices with cp.async, three K steps
+// ahead of the MMAs over five stages; one thread issues four tcgen05.mma (K = 16
 // each) into a 128 x 128 f32 accumulator in tensor memory and commits them to
 // the stage's mbarrier, which releases the stage for the next copies.  The
 // epilogue reads the accumulator with tcgen05.ld.
@@ -169,13 +169,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&p);
 }
 
+// Eight 4-bit codes (nibble i of wd is element i) -> bf16 (q - 8) * scale, in
+// element order, two elements per 32-bit word.  A code placed in the mantissa
+// of a bf16 whose exponent is that of 128 is the value 128 + q exactly (seven
+// mantissa bits hold q); subtracting 136 leaves q - 8 exactly, and the only
+// rounding is that of the product, as when (q - 8) * scale is formed in f32
+// (exactly: 4 + 8 significant bits) and rounded to bf16.  Word j below holds
+// elements j and j + 4; byte permutes put the pairs back in order.
+__device__ __forceinline__ uint4 int4x8_to_bf16(uint32_t wd, uint32_t scale2) {
+  const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&scale2);
+  const uint32_t off_bits = 0x43084308u;   // bf16x2 {136, 136}
+  const __nv_bfloat162 off = *reinterpret_cast<const __nv_bfloat162*>(&off_bits);
+  uint32_t v[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t p = ((wd >> (4 * j)) & 0x000F000Fu) | 0x43004300u;   // {128 + q_j, 128 + q_j+4}
+    const __nv_bfloat162 d = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162*>(&p), off), s2);
+    v[j] = *reinterpret_cast<const uint32_t*>(&d);
+  }
+  return make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
+                    __byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632));
+}
+
 // ------------------------------------------------------------------ GEMM
 // PH_UP: item = (tile, N tile nt of I / 64): B rows 0..63 are gate rows
 // nt*64 .., rows 64..127 the matching up rows; K = H.  Epilogue: h.
 // PH_DOWN: item = (tile, N tile nt of H / 128): B rows are W2 rows nt*128 ..;
 // K = I.  Epilogue: f32 output rows.
-constexpr int kGStagesP = 4;                 // staged K steps
-constexpr int kGAhead = 2;                   // K steps in flight ahead of the MMA
+constexpr int kGStagesP = 5;                 // staged K steps
+constexpr int kGAhead = 3;                   // K steps in flight ahead of the MMA
 constexpr int kRawBytes = kTileM * 2 * 32;   // raw INT4 (16 B per thread) or FP8 (32 B) rows of one K step
 constexpr int kMaxGroups = 64;               // scale groups per row kept in shared memory (K <= 8192)
 
@@ -339,18 +361,12 @@ __global__ void __launch_bounds__(kGThreads, 1) k_moe_gemm(GemmArgs g) {
       }
       if (F == MOE_INT4_G128) {
         const uint4 qv = *reinterpret_cast<const uint4*>(raw0 + (size_t)s * kRawBytes + (size_t)tid * kRawPer);
-        const float scl = bf16_bits(sc[r * kMaxGroups + ((ks * (int)tc::kTileK) >> 7)]);
+        const uint32_t sb = sc[r * kMaxGroups + ((ks * (int)tc::kTileK) >> 7)];
         const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t wd = words[i];   // elements 8 i .. 8 i + 7 of this thread's 32
-          uint4 o;
-          o.x = pack_bf16x2(code_m8(wd, 0) * scl, code_m8(wd, 4) * scl);
-          o.y = pack_bf16x2(code_m8(wd, 8) * scl, code_m8(wd, 12) * scl);
-          o.z = pack_bf16x2(code_m8(wd, 16) * scl, code_m8(wd, 20) * scl);
-          o.w = pack_bf16x2(code_m8(wd, 24) * scl, code_m8(wd, 28) * scl);
-          *reinterpret_cast<uint4*>(sbt + tc::tile_offset((uint32_t)r, (uint32_t)((hh * 4 + i) * 8))) = o;
-        }
+        for (int i = 0; i < 4; ++i)   // elements 8 i .. 8 i + 7 of this thread's 32
+          *reinterpret_cast<uint4*>(sbt + tc::tile_offset((uint32_t)r, (uint32_t)((hh * 4 + i) * 8))) =
+              int4x8_to_bf16(words[i], sb | (sb << 16));
       }
       tc::fence_async_smem();
       if (__syncthreads_or(dead)) {
