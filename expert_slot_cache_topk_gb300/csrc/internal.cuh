@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -151,6 +152,25 @@ cudaError_t launch_verify(const int32_t* slot_expert, int N, const uint8_t* pool
 
 // ---- moe_cache.cu: set the message moe_cache_last_error(NULL) returns ----
 moe_status set_global_error(moe_status st, const char* msg);
+
+// ---- moe_cache.cu: the canonical expert block, shared by every entry point ----
+// Byte sizes of the block's parts [w13 | w2 | s13 | s2] for a weight format and
+// shape; false if the format is unknown or the shape does not suit it.
+bool block_layout(int wdtype, int H, int I, size_t* w13, size_t* w2, size_t* s13, size_t* s2);
+// Elements per 16-byte chunk of a weight row (H and I must be multiples of it).
+int chunk_elems(int wdtype);
+// Kernel arguments for one grouped expert-MLP call, block offsets from block_layout.
+MlpArgs mlp_args(int wdtype, int H, int I, int k, const void* x, const unsigned long long* asg,
+                 const float* w, float* h, void* y, int T, int flags);
+
+// ---- moe_cache.cu: per-device launch state ----
+// Kernel attributes (the dynamic shared-memory opt-in, the carve-out) are set
+// per device, so every record of "already configured" is kept per device and
+// guarded by one mutex.
+constexpr int kMaxDevices = 64;
+int current_device();              // the current device, or -1 (none / index >= kMaxDevices)
+std::mutex& launch_state_mutex();
+int device_sm_count();             // multiprocessors of the current device (cached per device)
 
 // ---- launchers (k_mlp.cu) ----
 cudaError_t mlp_configure(int wdtype, int H, int I, int k);  // smem opt-in, call outside capture

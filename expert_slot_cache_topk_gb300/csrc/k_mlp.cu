@@ -450,8 +450,9 @@ struct Tiles<MOE_FP8_E4M3> {
   static constexpr int RP = 1, UU = 4, UD = 8;
 };
 
-// Opt a kernel into more than 48 KiB of dynamic shared memory once per size,
-// so launches (also inside stream capture) do not repeat the attribute call.
+// Opt a kernel into more than 48 KiB of dynamic shared memory once per size
+// and device, so launches (also inside stream capture) do not repeat the
+// attribute call.  Callers hold launch_state_mutex().
 template <typename K>
 cudaError_t allow_smem(K kernel, size_t bytes, size_t* configured) {
   if (bytes <= *configured) return cudaSuccess;
@@ -463,40 +464,23 @@ cudaError_t allow_smem(K kernel, size_t bytes, size_t* configured) {
   return e;
 }
 
-template <int F>
-struct Configured {
-  static size_t up, down, fused;
-  static int fused_blocks_per_sm;
-  static size_t fused_blocks_smem;
+// What has been configured for one weight format on one device.
+struct MlpLaunchState {
+  size_t up = 48 * 1024, down = 48 * 1024, fused = 48 * 1024;   // shared memory the attributes allow
+  int fused_blocks_per_sm = 0;                                   // occupancy of the fused kernel ...
+  size_t fused_blocks_smem = 0;                                  // ... at this shared-memory size
 };
-template <int F>
-size_t Configured<F>::up = 48 * 1024;
-template <int F>
-size_t Configured<F>::down = 48 * 1024;
-template <int F>
-size_t Configured<F>::fused = 48 * 1024;
-template <int F>
-int Configured<F>::fused_blocks_per_sm = 0;
-template <int F>
-size_t Configured<F>::fused_blocks_smem = 0;
+MlpLaunchState g_mlp_state[4][kMaxDevices];   // [weight format][device]
 
-constexpr int kMaxDev = 64;
-int g_sms[kMaxDev];
-
-int sm_count() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) dev = 0;
-  if (g_sms[dev] == 0) {
-    int v = 0;
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    g_sms[dev] = v > 0 ? v : 1;
-  }
-  return g_sms[dev];
+template <int F>
+MlpLaunchState* mlp_state() {
+  const int dev = current_device();
+  return dev < 0 ? nullptr : &g_mlp_state[F][dev];
 }
 
 // CTAs per token for the standalone kernels: two 16-warp CTAs per SM overall.
 int ctas_per_token(int T) {
-  const int g = 2 * sm_count() / (T > 0 ? T : 1);
+  const int g = 2 * device_sm_count() / (T > 0 ? T : 1);
   return g > 1 ? g : 1;
 }
 
@@ -508,22 +492,25 @@ size_t fused_smem(int H, int I, int k) {
 
 template <int F>
 cudaError_t configure_impl(int H, int I, int k) {
-  cudaError_t e = allow_smem(k_up<F, Tiles<F>::RP, Tiles<F>::UU>, mlp_up_smem_bytes(H), &Configured<F>::up);
+  device_sm_count();   // cache the SM count outside any capture
+  std::lock_guard<std::mutex> lock(launch_state_mutex());
+  MlpLaunchState* st = mlp_state<F>();
+  if (!st) return cudaErrorInvalidDevice;
+  cudaError_t e = allow_smem(k_up<F, Tiles<F>::RP, Tiles<F>::UU>, mlp_up_smem_bytes(H), &st->up);
   if (e != cudaSuccess) return e;
-  e = allow_smem(k_down<F, Tiles<F>::UD>, mlp_down_smem_bytes(k, I), &Configured<F>::down);
+  e = allow_smem(k_down<F, Tiles<F>::UD>, mlp_down_smem_bytes(k, I), &st->down);
   if (e != cudaSuccess) return e;
   auto fk = k_mlp_fused<F, Tiles<F>::RP, Tiles<F>::UU, Tiles<F>::UD>;
   const size_t fs = fused_smem<F>(H, I, k);
-  e = allow_smem(fk, fs, &Configured<F>::fused);
+  e = allow_smem(fk, fs, &st->fused);
   if (e != cudaSuccess) return e;
-  if (Configured<F>::fused_blocks_smem != fs) {
+  if (st->fused_blocks_smem != fs) {
     int nb = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fk, kMlpThreads, fs);
     if (e != cudaSuccess) return e;
-    Configured<F>::fused_blocks_per_sm = nb;
-    Configured<F>::fused_blocks_smem = fs;
+    st->fused_blocks_per_sm = nb;
+    st->fused_blocks_smem = fs;
   }
-  sm_count();
   return cudaSuccess;
 }
 
@@ -531,8 +518,13 @@ template <int F>
 cudaError_t up_impl(const MlpArgs& a, cudaStream_t s) {
   const size_t smem = mlp_up_smem_bytes(a.H);
   auto kern = k_up<F, Tiles<F>::RP, Tiles<F>::UU>;
-  cudaError_t e = allow_smem(kern, smem, &Configured<F>::up);
-  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(launch_state_mutex());
+    MlpLaunchState* st = mlp_state<F>();
+    if (!st) return cudaErrorInvalidDevice;
+    cudaError_t e = allow_smem(kern, smem, &st->up);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid(ctas_per_token(a.T), a.T);
   kern<<<grid, kMlpThreads, smem, s>>>(a);
   return cudaGetLastError();
@@ -542,8 +534,13 @@ template <int F>
 cudaError_t down_impl(const MlpArgs& a, cudaStream_t s) {
   const size_t smem = mlp_down_smem_bytes(a.k, a.I);
   auto kern = k_down<F, Tiles<F>::UD>;
-  cudaError_t e = allow_smem(kern, smem, &Configured<F>::down);
-  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(launch_state_mutex());
+    MlpLaunchState* st = mlp_state<F>();
+    if (!st) return cudaErrorInvalidDevice;
+    cudaError_t e = allow_smem(kern, smem, &st->down);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid(ctas_per_token(a.T), a.T);
   kern<<<grid, kMlpThreads, smem, s>>>(a);
   return cudaGetLastError();
@@ -552,9 +549,15 @@ cudaError_t down_impl(const MlpArgs& a, cudaStream_t s) {
 template <int F>
 cudaError_t fused_impl(const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s) {
   const size_t smem = fused_smem<F>(a.H, a.I, a.k);
-  if (Configured<F>::fused_blocks_smem != smem || Configured<F>::fused_blocks_per_sm < 1)
-    return cudaErrorNotSupported;      // not configured for this shape: caller falls back
-  const int grid = Configured<F>::fused_blocks_per_sm * sm_count();
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(launch_state_mutex());
+    const MlpLaunchState* st = mlp_state<F>();
+    if (!st || st->fused_blocks_smem != smem || st->fused_blocks_per_sm < 1)
+      return cudaErrorNotSupported;    // not configured for this shape: caller falls back
+    per_sm = st->fused_blocks_per_sm;
+  }
+  const int grid = per_sm * device_sm_count();
   if (a.T > grid) return cudaErrorNotSupported;
   auto kern = k_mlp_fused<F, Tiles<F>::RP, Tiles<F>::UU, Tiles<F>::UD>;
   MlpArgs args = a;

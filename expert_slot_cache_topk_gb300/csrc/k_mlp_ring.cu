@@ -1047,48 +1047,36 @@ bool ring_geometry(int F, int H, int I, int k, RingCfg* rc, size_t* dyn_smem) {
   return true;
 }
 
-template <int F>
-struct RingState {
-  static size_t smem;        // dynamic shared memory the attribute allows
-  static int blocks_per_sm;  // occupancy at that size
+// Shared memory the attribute allows and the occupancy at that size, per
+// weight format and device (guarded by launch_state_mutex()).
+struct RingLaunchState {
+  size_t smem = 0;
+  int blocks_per_sm = 0;
 };
-template <int F>
-size_t RingState<F>::smem = 0;
-template <int F>
-int RingState<F>::blocks_per_sm = 0;
-
-constexpr int kMaxDev = 64;
-int g_sms[kMaxDev];
-
-int sm_count() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) dev = 0;
-  if (g_sms[dev] == 0) {
-    int v = 0;
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    g_sms[dev] = v > 0 ? v : 1;
-  }
-  return g_sms[dev];
-}
+RingLaunchState g_ring_state[4][kMaxDevices];
 
 template <int F>
 cudaError_t ring_configure_impl(int H, int I, int k) {
   RingCfg rc;
   size_t smem = 0;
   if (!ring_geometry(F, H, I, k, &rc, &smem)) return cudaSuccess;   // not used for this shape
-  if (RingState<F>::smem < smem) {
+  device_sm_count();   // cache the SM count outside any capture
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(launch_state_mutex());
+  RingLaunchState& st = g_ring_state[F][dev];
+  if (st.smem < smem) {
     cudaError_t e = cudaFuncSetAttribute(k_mlp_ring<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k_mlp_ring<F>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    RingState<F>::smem = smem;
+    st.smem = smem;
   }
   int nb = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_mlp_ring<F>, kRingThreads, smem);
   if (e != cudaSuccess) return e;
-  RingState<F>::blocks_per_sm = nb;
-  sm_count();
+  st.blocks_per_sm = nb;
   return cudaSuccess;
 }
 
@@ -1097,11 +1085,17 @@ cudaError_t ring_impl(const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s) 
   RingCfg rc;
   size_t smem = 0;
   if (a.T != 1 || !ring_geometry(F, a.H, a.I, a.k, &rc, &smem)) return cudaErrorNotSupported;
-  if (RingState<F>::smem < smem || RingState<F>::blocks_per_sm < 1) return cudaErrorNotSupported;
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorNotSupported;
+  {
+    std::lock_guard<std::mutex> lock(launch_state_mutex());
+    const RingLaunchState& st = g_ring_state[F][dev];
+    if (st.smem < smem || st.blocks_per_sm < 1) return cudaErrorNotSupported;
+  }
   MlpArgs args = a;
   void* params[] = {&args, &rc, &bar, &err};
-  return cudaLaunchCooperativeKernel((const void*)k_mlp_ring<F>, dim3(sm_count()), dim3(kRingThreads), params,
-                                     smem, s);
+  return cudaLaunchCooperativeKernel((const void*)k_mlp_ring<F>, dim3(device_sm_count()), dim3(kRingThreads),
+                                     params, smem, s);
 }
 
 }  // namespace

@@ -486,26 +486,22 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ out, 
 constexpr size_t kGemmSmem = (size_t)kGStagesP * (kGStageBytes + kRawBytes) +
                              (size_t)kTileM * kMaxGroups * 2 + 1024;   // + alignment slack
 
-template <int F>
-struct GemmState {
-  static bool configured;
-  static int blocks_per_sm;
+// Whether the attributes are set and the occupancy, per weight format and
+// device (guarded by launch_state_mutex()).
+struct GemmLaunchState {
+  bool configured = false;
+  int blocks_per_sm = 0;
 };
-template <int F>
-bool GemmState<F>::configured = false;
-template <int F>
-int GemmState<F>::blocks_per_sm = 0;
-
-int dev_sms() {
-  int dev = 0, v = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-  return v > 0 ? v : 1;
-}
+GemmLaunchState g_gemm_state[4][kMaxDevices];
 
 template <int F>
 cudaError_t gemm_configure_impl() {
-  if (GemmState<F>::configured) return cudaSuccess;
+  device_sm_count();   // cache the SM count outside any capture
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(launch_state_mutex());
+  GemmLaunchState& st = g_gemm_state[F][dev];
+  if (st.configured) return cudaSuccess;
   const void* kernels[] = {(const void*)k_moe_gemm<F, PH_UP>, (const void*)k_moe_gemm<F, PH_DOWN>};
   for (const void* kf : kernels) {
     cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
@@ -513,18 +509,25 @@ cudaError_t gemm_configure_impl() {
       e = cudaFuncSetAttribute(kf, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e;
   int nb = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_moe_gemm<F, PH_UP>, kGThreads, kGemmSmem);
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_moe_gemm<F, PH_UP>, kGThreads, kGemmSmem);
   if (e != cudaSuccess) return e;
-  GemmState<F>::blocks_per_sm = nb;
-  GemmState<F>::configured = true;
+  st.blocks_per_sm = nb;
+  st.configured = true;
   return cudaSuccess;
 }
 
 template <int F>
 cudaError_t gemm_impl(const MlpArgs& a, const GemmBuffers& b, cudaStream_t s) {
-  if (!GemmState<F>::configured || GemmState<F>::blocks_per_sm < 1) return cudaErrorNotSupported;
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorNotSupported;
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(launch_state_mutex());
+    const GemmLaunchState& st = g_gemm_state[F][dev];
+    if (!st.configured || st.blocks_per_sm < 1) return cudaErrorNotSupported;
+    per_sm = st.blocks_per_sm;
+  }
   const int n = a.T * a.k;
   k_group<<<1, kGroupThreads, 0, s>>>(b.ids, n, b.E, b.order, b.tiles, b.ntiles, b.work);
   cudaError_t e = cudaGetLastError();
@@ -549,7 +552,7 @@ cudaError_t gemm_impl(const MlpArgs& a, const GemmBuffers& b, cudaStream_t s) {
   g.pending = b.pending;
   g.ready = b.ready;
   g.hdr = b.hdr;
-  const int grid = GemmState<F>::blocks_per_sm * dev_sms();
+  const int grid = per_sm * device_sm_count();
   k_moe_gemm<F, PH_UP><<<grid, kGThreads, kGemmSmem, s>>>(g);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -37,7 +37,11 @@ constexpr int kDefaultTimingCap = 4096;
 
 size_t round_up(size_t v, size_t m) { return (v + m - 1) / m * m; }
 
-bool layout(int wd, int H, int I, size_t* w13, size_t* w2, size_t* s13, size_t* s2) {
+size_t act_bytes(int wd) { return wd == MOE_F32 ? 4 : 2; }
+
+}  // namespace
+
+bool moe::block_layout(int wd, int H, int I, size_t* w13, size_t* w2, size_t* s13, size_t* s2) {
   const size_t h = (size_t)H, i = (size_t)I;
   switch (wd) {
     case MOE_F32: *w13 = 2 * i * h * 4; *w2 = h * i * 4; *s13 = *s2 = 0; return true;
@@ -55,12 +59,55 @@ bool layout(int wd, int H, int I, size_t* w13, size_t* w2, size_t* s13, size_t* 
   return false;
 }
 
-int chunk_elems(int wd) {
+int moe::chunk_elems(int wd) {
   return wd == MOE_F32 ? 4 : (wd == MOE_BF16 ? 8 : (wd == MOE_FP8_E4M3 ? 16 : 32));
 }
-size_t act_bytes(int wd) { return wd == MOE_F32 ? 4 : 2; }
 
+MlpArgs moe::mlp_args(int wd, int H, int I, int k, const void* x, const unsigned long long* asg,
+                      const float* w, float* h, void* y, int T, int flags) {
+  size_t w13 = 0, w2 = 0, s13 = 0, s2 = 0;
+  block_layout(wd, H, I, &w13, &w2, &s13, &s2);
+  MlpArgs a{};
+  a.x = x;
+  a.asg_ptr = asg;
+  a.w = w;
+  a.h = h;
+  a.y = y;
+  a.T = T;
+  a.k = k;
+  a.H = H;
+  a.I = I;
+  a.residual = (flags & MOE_FWD_RESIDUAL) ? 1 : 0;
+  a.off_w2 = w13;
+  a.off_s13 = w13 + w2;
+  a.off_s2 = w13 + w2 + s13;
+  return a;
+}
+
+namespace {
+std::mutex g_launch_state_mu;
+int g_device_sms[moe::kMaxDevices];
 }  // namespace
+
+int moe::current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+std::mutex& moe::launch_state_mutex() { return g_launch_state_mu; }
+
+int moe::device_sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  std::lock_guard<std::mutex> lock(g_launch_state_mu);
+  if (g_device_sms[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    g_device_sms[dev] = v > 0 ? v : 1;
+  }
+  return g_device_sms[dev];
+}
 
 struct moe_cache {
   moe_cache_config cfg{};
@@ -476,27 +523,6 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
   return MOE_OK;
 }
 
-MlpArgs mlp_args(int wd, int H, int I, int k, const void* x, const unsigned long long* asg,
-                 const float* w, float* h, void* y, int T, int flags) {
-  size_t w13, w2, s13, s2;
-  layout(wd, H, I, &w13, &w2, &s13, &s2);
-  MlpArgs a{};
-  a.x = x;
-  a.asg_ptr = asg;
-  a.w = w;
-  a.h = h;
-  a.y = y;
-  a.T = T;
-  a.k = k;
-  a.H = H;
-  a.I = I;
-  a.residual = (flags & MOE_FWD_RESIDUAL) ? 1 : 0;
-  a.off_w2 = w13;
-  a.off_s13 = w13 + w2;
-  a.off_s2 = w13 + w2 + s13;
-  return a;
-}
-
 moe_status measure_copy_modes(moe_cache* c) {
   // Time a pinned-host -> HBM copy both ways on the handle's own buffers.
   // (layer 0's pool or the scratch, from layer 0's backing store: contiguous in either table layout)
@@ -614,7 +640,7 @@ const char* moe_cache_last_error(const moe_cache_t* c) {
 
 moe_status moe_cache_expert_bytes(int wdtype, int hidden, int inter, size_t* bytes) {
   size_t a, b, s1, s2;
-  if (!bytes || hidden <= 0 || inter <= 0 || !layout(wdtype, hidden, inter, &a, &b, &s1, &s2))
+  if (!bytes || hidden <= 0 || inter <= 0 || !block_layout(wdtype, hidden, inter, &a, &b, &s1, &s2))
     return fail(nullptr, MOE_EINVAL, "bad weight format or shape");
   *bytes = a + b + s1 + s2;
   return MOE_OK;
@@ -634,7 +660,7 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   if (g.max_tokens < 1 || (long long)g.max_tokens * g.top_k > 65535)
     return fail(nullptr, MOE_EINVAL, "need max_tokens >= 1 and max_tokens * top_k <= 65535");
   size_t w13, w2, s13, s2;
-  if (g.hidden <= 0 || g.inter <= 0 || !layout(g.wdtype, g.hidden, g.inter, &w13, &w2, &s13, &s2))
+  if (g.hidden <= 0 || g.inter <= 0 || !block_layout(g.wdtype, g.hidden, g.inter, &w13, &w2, &s13, &s2))
     return fail(nullptr, MOE_EINVAL, "bad wdtype or shape (int4 needs hidden, inter multiples of 128; fp8 of 16)");
   if (g.hidden % chunk_elems(g.wdtype) || g.inter % chunk_elems(g.wdtype))
     return fail(nullptr, MOE_EINVAL, "hidden and inter must be multiples of 4 (f32), 8 (bf16) or 16 (fp8)");
@@ -940,7 +966,7 @@ moe_status moe_expert_mlp(int wdtype, int hidden, int inter, int top_k, const vo
                           const uint64_t* block_ptrs_d, const float* w_d, int T,
                           float* h_scratch_d, void* y_d, int flags, moe_stream_t stream) {
   size_t a1, a2, a3, a4;
-  if (!layout(wdtype, hidden, inter, &a1, &a2, &a3, &a4) || hidden % chunk_elems(wdtype) ||
+  if (!block_layout(wdtype, hidden, inter, &a1, &a2, &a3, &a4) || hidden % chunk_elems(wdtype) ||
       inter % chunk_elems(wdtype))
     return fail(nullptr, MOE_EINVAL, "bad weight format or shape");
   if (top_k < 1 || top_k > MOE_MAX_TOPK || T < 0 || (long long)T * top_k > 65535)

@@ -3,12 +3,11 @@
 //
 // The regular entry point takes the gate/up intermediate h (T*k*I floats)
 // from a buffer the caller allocates.  Some callers have no way to do that at
-// the point of the call: code that runs while a CUDA graph is being captured
-// (cudaMalloc is not allowed there), plugins hosted by a framework whose
-// caching allocator owns every byte of device memory, and latency-critical
-// loops that must never hit cudaMalloc's implicit device synchronisation.
-// This variant keeps its scratch in a fixed-size array compiled into the
-// library instead, so a call allocates nothing.
+// the point of the call: plugins hosted by a framework whose caching
+// allocator owns every byte of device memory, and latency-critical loops that
+// must never hit cudaMalloc's implicit device synchronisation.  This variant
+// keeps its scratch in a fixed-size array compiled into the library instead,
+// so a call allocates nothing.
 //
 // Costs and rules for users:
 //  * The array (MOE_NOALLOC_MAX_SCRATCH_FLOATS floats, 2 MiB) exists on every
@@ -22,6 +21,10 @@
 //  * The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (a one-time set-up per device, done with that device
 //    current).  Make that first call before any stream capture.
+//
+// Shape checks, the expert block layout and the kernels are the ones
+// moe_expert_mlp uses (block_layout / chunk_elems / mlp_args), so both entry
+// points accept the same shapes and give the same bits.
 
 #include <cuda_runtime.h>
 
@@ -35,7 +38,6 @@ namespace {
 
 static __device__ __align__(256) float g_mlp_scratch[MOE_NOALLOC_MAX_SCRATCH_FLOATS];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 float* g_scratch_ptr[kMaxDevices] = {};
 
@@ -43,14 +45,12 @@ float* g_scratch_ptr[kMaxDevices] = {};
 // symbol name itself is only a host-side stand-in, so it must never be passed
 // to a kernel; the address comes from cudaGetSymbolAddress, once per device.
 cudaError_t scratch_on_current_device(float** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_mlp_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_mlp_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_ptr[dev] = static_cast<float*>(p);
   }
@@ -58,19 +58,16 @@ cudaError_t scratch_on_current_device(float** out) {
   return cudaSuccess;
 }
 
-int chunk_elems(int wd) { return wd == MOE_F32 ? 4 : (wd == MOE_BF16 ? 8 : 32); }
-
 }  // namespace
 
 extern "C" moe_status moe_expert_mlp_noalloc(int wdtype, int hidden, int inter, int top_k,
                                              const void* x_d, const uint64_t* block_ptrs_d,
                                              const float* w_d, int T, void* y_d, int flags,
                                              moe_stream_t stream) {
-  if (wdtype != MOE_F32 && wdtype != MOE_BF16 && wdtype != MOE_INT4_G128 && wdtype != MOE_FP8_E4M3)
-    return set_global_error(MOE_EINVAL, "moe_expert_mlp_noalloc: bad wdtype");
-  if (hidden <= 0 || inter <= 0 || hidden % chunk_elems(wdtype) || inter % chunk_elems(wdtype) ||
-      (wdtype == MOE_INT4_G128 && (hidden % 128 || inter % 128)))
-    return set_global_error(MOE_EINVAL, "moe_expert_mlp_noalloc: bad hidden/inter for this format");
+  size_t w13 = 0, w2 = 0, s13 = 0, s2 = 0;
+  if (!block_layout(wdtype, hidden, inter, &w13, &w2, &s13, &s2) || hidden <= 0 || inter <= 0 ||
+      hidden % chunk_elems(wdtype) || inter % chunk_elems(wdtype))
+    return set_global_error(MOE_EINVAL, "moe_expert_mlp_noalloc: bad weight format or shape");
   if (top_k < 1 || top_k > MOE_MAX_TOPK || T < 0 || (long long)T * top_k > 65535)
     return set_global_error(MOE_EINVAL, "moe_expert_mlp_noalloc: bad top_k or T");
   if (mlp_up_smem_bytes(hidden) > 200 * 1024 || mlp_down_smem_bytes(top_k, inter) > 200 * 1024)
@@ -91,26 +88,10 @@ extern "C" moe_status moe_expert_mlp_noalloc(int wdtype, int hidden, int inter, 
   e = mlp_configure(wdtype, hidden, inter, top_k);
   if (e != cudaSuccess) return set_global_error(MOE_ECUDA, cudaGetErrorString(e));
 
-  MlpArgs a{};
-  a.x = x_d;
-  a.asg_ptr = reinterpret_cast<const unsigned long long*>(block_ptrs_d);
-  a.w = w_d;
-  a.h = h;
-  a.y = y_d;
-  a.T = T;
-  a.k = top_k;
-  a.H = hidden;
-  a.I = inter;
-  a.residual = (flags & MOE_FWD_RESIDUAL) ? 1 : 0;
-  const size_t H = (size_t)hidden, I = (size_t)inter;
-  size_t w13, w2, s13;
-  if (wdtype == MOE_F32) { w13 = 2 * I * H * 4; w2 = H * I * 4; s13 = 0; }
-  else if (wdtype == MOE_BF16) { w13 = 2 * I * H * 2; w2 = H * I * 2; s13 = 0; }
-  else { w13 = 2 * I * H / 2; w2 = H * I / 2; s13 = 2 * I * (H / 128) * 2; }
-  a.off_w2 = w13;
-  a.off_s13 = w13 + w2;
-  a.off_s2 = w13 + w2 + s13;
-  cudaStream_t s = (cudaStream_t)stream;
+  const MlpArgs a = mlp_args(wdtype, hidden, inter, top_k, x_d,
+                             reinterpret_cast<const unsigned long long*>(block_ptrs_d), w_d, h, y_d, T,
+                             flags);
+  const cudaStream_t s = (cudaStream_t)stream;
   e = launch_mlp_up(wdtype, a, s);
   if (e == cudaSuccess) e = launch_mlp_down(wdtype, a, s);
   if (e != cudaSuccess) return set_global_error(MOE_ECUDA, cudaGetErrorString(e));

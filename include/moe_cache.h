@@ -342,13 +342,13 @@ moe_status moe_expert_mlp(int wdtype, int hidden, int inter, int top_k,
 
 /* Allocation-free variant of moe_expert_mlp (the pages have no counterpart;
  * this entry point exists for callers of this library that cannot allocate
- * device memory where they call it: code running under CUDA graph capture,
- * plugins whose host framework's caching allocator owns all device memory,
- * and latency-critical loops that must not hit cudaMalloc's implicit device
- * synchronisation).  Same arguments, arithmetic and results as
- * moe_expert_mlp, minus h_scratch_d: the intermediate h lives in a 2 MiB
- * array compiled into the library, which every GPU that loads the library
- * holds until the process exits.  The call allocates nothing.
+ * device memory where they call it: plugins whose host framework's caching
+ * allocator owns all device memory, and latency-critical loops that must not
+ * hit cudaMalloc's implicit device synchronisation).  Same arguments, shape
+ * rules, block layout, arithmetic and results as moe_expert_mlp, minus
+ * h_scratch_d: the intermediate h lives in a 2 MiB array compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  The call allocates nothing.
  *  - Rejects T * top_k * inter > MOE_NOALLOC_MAX_SCRATCH_FLOATS (MOE_EINVAL).
  *  - All calls on a device share the array and it keeps the last call's
  *    contents (nothing in it needs to start at zero); calls whose kernels
