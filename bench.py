@@ -8,6 +8,18 @@ libmoecache.so kernels.  Inputs (routing logits and hidden states of every
 step) are resident in HBM before the timed region; every step reads 1.61 GB of
 expert weights, far more than the 129 MB L2, so no flush is needed.
 
+The same line carries the other workloads of the path, each measured the
+same way (warm-up steps, then the timed steps replayed from an uploaded CUDA
+graph from the warmed state):
+  int4_decode     Flash-Next-shaped INT4 g128 decode (16 layers x 512 experts,
+                  top-10) at pool sizes N = 0, 16, 32, 64, plus every expert
+                  resident (the staged kernel's roofline without misses)
+  batched_decode  64 sequences per step on the INT4 shapes, N = 64 (most steps
+                  bypass the pool), and every expert resident (the grouped
+                  tensor-core GEMM alone)
+  prefill         a 2048-token prefill chunk (bypass) with the cold set read in
+                  place, then batch-1 decode on the same cache
+
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
 Prints one JSON line.  Under torchrun each rank runs an independent replica
@@ -25,6 +37,7 @@ import subprocess
 import sys
 import threading
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -35,6 +48,7 @@ from expert_slot_cache_topk_gb300 import synth  # noqa: E402
 
 METRIC = "MoE decode tok/s with slot cache; miss H2D GB/s and GEMM HBM GB/s vs roof"
 UNIT = "tok/s"
+DATA = "synthetic (seeded Zipf routing with reuse; N(0,0.02) weights)"
 
 
 # ---------------------------------------------------------------------------
@@ -124,11 +138,10 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# workload
+# workloads, peaks, the profiled-traffic table
 # ---------------------------------------------------------------------------
 
-# arithmetic of the decode path per weight format: weights decoded to f32 in
-# registers, f32 accumulation, bf16 activations (f32 for f32 weights)
+# arithmetic of the decode path per weight format
 DTYPE_NAME = {"bf16": "bf16", "f32": "f32", "fp8": "fp8_e4m3 weights, bf16 activations",
               "int4g128": "int4_g128 weights, bf16 activations"}
 
@@ -138,6 +151,15 @@ def workload_desc(w) -> str:
             f"hidden {w.hidden}, expert inter {w.inter}, {w.wdtype} weights, {w.slots} slots/layer, "
             f"batch {w.tokens}, routing {w.routing} Zipf({w.zipf_s})"
             + (f" with p={w.reuse_p} reuse" if w.reuse_p else ""))
+
+
+def run_config(w, world: int) -> dict:
+    """The `config` of the JSON line: the workload only, identical in both arms."""
+    lay = synth.expert_layout(w.wdtype, w.hidden, w.inter)
+    return {"workload": workload_desc(w), "tokens_per_step": w.tokens,
+            "l2": "inputs larger than L2: every step reads "
+                  f"{w.layers * w.top_k * w.tokens * lay['total'] / 1e9:.2f} GB of expert weights",
+            "parallelism": f"replicas x{world}"}
 
 
 def peaks() -> dict:
@@ -150,20 +172,21 @@ def peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-# DRAM bytes per launch of the roofline kernel from an ncu capture
-# (profiles/k_mlp_ring_olmoe_decode_nomiss.md), valid only while the kernel
-# source is the one that was profiled.
+# DRAM bytes (read + write) per launch of a staged-kernel launch without
+# misses, from ncu captures of the source whose tag is the key (null once the
+# kernel source differs from the profiled one).
 MEASURED_TRAFFIC = {
     ("olmoe", "k_mlp_ring.cu:d08a8647eee599d1"): 103_437_312,
 }
 
 
 def kernel_source_tag() -> str:
-    """Hash of the roofline kernel's code and the shared header it includes.
+    """Hash of the staged kernel's code and the shared header it includes.
 
     Line comments and blank lines are left out, so that a change of wording
     in a comment keeps the tag of the measured traffic."""
-    import hashlib, re
+    import hashlib
+    import re
     h = hashlib.sha256()
     for name in ("k_mlp_ring.cu", "mlp_common.cuh"):
         with open(os.path.join(ROOT, "expert_slot_cache_topk_gb300", "csrc", name), encoding="utf-8") as f:
@@ -239,6 +262,72 @@ def oracle_tokens_per_s(w, tokens: int = 2, budget_s: float = 20.0):
     return (done / w.layers) * w.tokens / spent, done, spent
 
 
+def oracle_integer_trace(w, layers=None) -> dict:
+    """The oracle's integer path alone (router top-k + the slot pool) over the
+    workload's full decode trace: every step of `layers` (default: all).
+    Logit generation is outside the timed part."""
+    from oracle import LayerSlotCache, expert_nbytes, router_topk
+    Be = expert_nbytes(w.wdtype, w.hidden, w.inter)["total"]
+    ls = list(range(w.layers if layers is None else min(layers, w.layers)))
+    spent = 0.0
+    for l in ls:
+        lg = synth.routing_logits(w, l, w.steps)
+        cm = synth.cold_mask(w, l) if w.cold_frac > 0 else None
+        c = LayerSlotCache(w.experts, w.slots, Be, cm)
+        t0 = time.perf_counter()
+        for s in range(w.steps):
+            ids, _ = router_topk(lg[s], w.top_k)
+            c.prepare(ids)
+        spent += time.perf_counter() - t0
+    n = len(ls) * w.steps
+    return {"workload": w.name, "slots": w.slots, "steps": w.steps, "layers": len(ls),
+            "layer_steps": n, "seconds": spent, "layer_steps_per_s": n / spent,
+            "tokens_per_s": n / w.layers * w.tokens / spent}
+
+
+def oracle_child(workload: str, budget: float):
+    """Single-core oracle timing, run in a child process whose BLAS threads are
+    pinned to 1 by the environment the parent sets before numpy loads."""
+    try:
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+    except (AttributeError, OSError):
+        pass
+    w = synth.WORKLOADS[workload]
+    v, n, dt = oracle_tokens_per_s(w, 2, budget_s=budget)
+    print(json.dumps({"value": v, "layer_steps": n, "seconds": dt, "cores": cpu_cores()}), flush=True)
+
+
+def oracle_single_core(workload: str, budget: float):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", workload,
+                            "--cpu-budget", str(budget)], env=env, capture_output=True, text=True,
+                           timeout=budget * 6 + 120)
+        for ln in r.stdout.splitlines():
+            if ln.startswith("{"):
+                return json.loads(ln)
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return None
+
+
+def cpu_baseline(w, budget: float) -> dict:
+    """The oracle as it stands on the host cores: the float path on a bounded
+    sample with all cores (BLAS threads as installed) and on one core, and the
+    integer path (router + slot pool) over the full 512-step traces."""
+    v, n, dt = oracle_tokens_per_s(w, 2, budget_s=budget)
+    one = oracle_single_core(w.name, budget)
+    traces = [oracle_integer_trace(synth.WORKLOADS[name]) for name in ("tiny", "olmoe", "int4", "prefill_cold")]
+    traces.append(oracle_integer_trace(synth.WORKLOADS["batched"], layers=2))
+    return {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} (token, layer) steps of the first 2 decode tokens in {dt:.1f} s "
+                      f"(float64 numpy, BLAS threads as installed)",
+            "single_core": (dict(one, unit=UNIT, cores=1,
+                                 sample=f"{one['layer_steps']} (token, layer) steps in {one['seconds']:.1f} s, "
+                                        "one core, BLAS threads 1") if one else None),
+            "integer_trace": traces}
+
+
 def run_reference(args, w):
     rank, _, world = dist_env()
     if world > 1:
@@ -259,8 +348,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded Zipf routing with reuse; N(0,0.02) weights)",
-        "config": {"workload": workload_desc(w)},
+        "data": DATA, "config": run_config(w, args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -272,7 +360,54 @@ def run_reference(args, w):
 
 
 # ---------------------------------------------------------------------------
-# our arm
+# weights
+# ---------------------------------------------------------------------------
+
+class Int4Weights:
+    """The INT4 g128 expert blocks of the Flash-Next-shaped workload, generated
+    once and copied into every INT4 handle of the run (the INT4 decode sweep,
+    batched decode and the prefill chunk share these shapes; their routing is
+    each workload's own)."""
+
+    def __init__(self):
+        self.w = synth.WORKLOADS["int4"]
+        lay = synth.expert_layout(self.w.wdtype, self.w.hidden, self.w.inter)
+        self.stride = (lay["total"] + 255) // 256 * 256
+        self.layers = {}
+        self.gen_s = 0.0
+
+    def layer(self, l: int) -> np.ndarray:
+        if l not in self.layers:
+            t0 = time.time()
+            buf = np.empty((self.w.experts, self.stride), np.uint8)
+            synth.fill_layer_blocks(self.w, l, buf.reshape(-1), self.stride)
+            self.layers[l] = buf
+            self.gen_s += time.time() - t0
+        return self.layers[l]
+
+    def fill(self, c, layers: int):
+        assert c.info()["slot_stride"] == self.stride
+
+        def one(l):
+            np.copyto(c.backing_view(l), self.layer(l))
+
+        for l in range(layers):
+            self.layer(l)
+        with ThreadPoolExecutor(8) as ex:
+            list(ex.map(one, range(layers)))
+
+
+def fill_weights(c, w, int4src=None):
+    if int4src is not None and (w.wdtype, w.experts, w.hidden, w.inter) == ("int4g128", 512, 2560, 640):
+        int4src.fill(c, w.layers)
+        return
+    stride = c.info()["slot_stride"]
+    for l in range(w.layers):
+        synth.fill_layer_blocks(w, l, c.backing_view(l).reshape(-1), stride)
+
+
+# ---------------------------------------------------------------------------
+# one decode workload through the library, graph-replayed
 # ---------------------------------------------------------------------------
 
 def _fit_per_miss(ms: np.ndarray, misses: np.ndarray):
@@ -284,26 +419,262 @@ def _fit_per_miss(ms: np.ndarray, misses: np.ndarray):
     return float(base), float(per)
 
 
-def run_prefill(args, dev, world):
-    """Prefill chunk of the prefill + cold-set workload: all layers of one
-    2048-token chunk through moe_forward (the bypass path: every non-cold
-    expert of the chunk is copied to scratch, cold experts are read in place,
-    the grouped expert MLP runs on the tensor cores).  Returns the JSON
-    object, or None when skipped."""
-    import torch
-    from expert_slot_cache_topk_gb300._abi import MOE_FWD_RESIDUAL, MoECache
-    w = synth.WORKLOADS["prefill_cold"]
+class DecodeRun:
+    """Steps of one workload on one handle: inputs resident in HBM, each step
+    writes its own output buffers, so the timed steps replay from one graph."""
+
+    def __init__(self, c, w, dev, warmup: int, steps: int, graph: bool = True):
+        import torch
+        from expert_slot_cache_topk_gb300._abi import MOE_FWD_RESIDUAL
+        self.c, self.w, self.dev = c, w, dev
+        self.warmup, self.steps = warmup, steps
+        S = warmup + steps
+        self.lg = np.stack([synth.routing_logits(w, l, S) for l in range(w.layers)], axis=1)   # [S, L, T, E]
+        self.x0 = synth.hidden_states(w, 0, S)                                                 # [S, T, H]
+        self.lg_d = torch.from_numpy(self.lg).to(dev)
+        if w.wdtype == "f32":
+            self.x0_d = torch.from_numpy(self.x0).to(dev)
+            ydt = torch.float32
+        else:
+            self.x0_d = torch.from_numpy(self.x0.view(np.int16)).to(dev).view(torch.bfloat16)
+            ydt = torch.bfloat16
+        self.ys = torch.empty((S, w.layers, w.tokens, w.hidden), dtype=ydt, device=dev)
+        self.stream = torch.cuda.Stream(dev)
+        self.flag = MOE_FWD_RESIDUAL
+        # MEMCPY mode takes a host decision per layer step, so it cannot be captured
+        self.use_graph = graph and c.info()["copy_mode_name"] != "memcpy"
+
+    def step(self, s):
+        x = self.x0_d[s]
+        for l in range(self.w.layers):
+            self.c.forward(l, x, self.lg_d[s, l], self.w.tokens, self.ys[s, l], self.flag, self.stream)
+            x = self.ys[s, l]
+
+    def warm(self):
+        import torch
+        self.c.reset()
+        with torch.cuda.stream(self.stream):
+            for s in range(self.warmup):
+                self.step(s)
+        self.stream.synchronize()
+
+    def prime(self, timing: bool):
+        """Empty the pools, run the warm-up steps, then capture (or not) the
+        timed steps; returns (graph or None, kernel launches of the timed
+        steps).  The uninstrumented graph is replayed once untimed (its first
+        launch uploads it to the device), then the pools are emptied and warmed
+        up again, so that the timed replay starts from the state the capture
+        saw."""
+        import torch
+        self.warm()
+        self.c.set_timing(timing, capacity=self.steps * self.w.layers + 64)
+        l0 = self.c.info()["kernel_launches"]
+        g = None
+        if self.use_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.stream):
+                with torch.cuda.graph(g, stream=self.stream):
+                    for s in range(self.warmup, self.warmup + self.steps):
+                        self.step(s)
+            self.stream.synchronize()
+            n = self.c.info()["kernel_launches"] - l0
+            if not timing:
+                with torch.cuda.stream(self.stream):
+                    g.replay()
+                self.stream.synchronize()
+                self.warm()
+            return g, n
+        return g, 0
+
+    def timed(self, g, world, sampler_ms=0, local_rank=0):
+        """Run the timed steps once; (seconds, kernel launches, clock summary)."""
+        import torch
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0 = self.c.info()["kernel_launches"]
+        clk = ClockSampler(local_rank, sampler_ms)
+        with (clk if sampler_ms > 0 else contextlib.nullcontext()):
+            barrier(world)
+            torch.cuda.synchronize(self.dev)
+            with torch.cuda.stream(self.stream):
+                ev0.record(self.stream)
+                if g is not None:
+                    g.replay()
+                else:
+                    for s in range(self.warmup, self.warmup + self.steps):
+                        self.step(s)
+                ev1.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            barrier(world)
+        return (ev0.elapsed_time(ev1) / 1e3, self.c.info()["kernel_launches"] - l0,
+                clk.summary() if sampler_ms > 0 else None)
+
+    def measure(self, world, sampler_ms=0, local_rank=0) -> dict:
+        """The uninstrumented timed replay (throughput, counters), then the same
+        steps from the same state with per-launch events (kernel roofline,
+        copy spans, phase split)."""
+        g, launches = self.prime(False)
+        st0 = self.c.stats(-1)
+        sec, eager_launches, clocks = self.timed(g, world, sampler_ms, local_rank)
+        st1 = self.c.stats(-1)
+        del g
+        gt, _ = self.prime(True)
+        self.timed(gt, world)
+        del gt
+        tm = self.c.read_timing()
+        mlp_ms, mlp_miss = self.c.read_timing_launches()
+        spans = self.c.read_copy_spans()
+        self.c.set_timing(False)
+        return {"sec": sec, "launches": launches if self.use_graph else eager_launches, "clocks": clocks,
+                "st0": st0, "st1": st1, "tm": tm, "mlp_ms": mlp_ms, "mlp_miss": mlp_miss, "spans": spans}
+
+
+def kernel_roofline(w, r: dict, pk: dict) -> dict:
+    """HBM roofline of the expert-MLP kernel over the launches that copied
+    nothing (no miss, no bypass): every byte of the k experts' blocks is read
+    from HBM once per launch."""
+    lay = synth.expert_layout(w.wdtype, w.hidden, w.inter)
+    bytes_hbm = w.tokens * w.top_k * lay["total"]
+    ms, miss = r["mlp_ms"], r["mlp_miss"]
+    sp = r["spans"]
+    copied = sp[:, 2] if len(sp) == len(ms) else np.zeros(len(ms), np.uint64)   # bypass steps copy with 0 misses
+    hit_ms = ms[(miss == 0) & (copied == 0) & (ms > 0)]
+    hit_us = float(hit_ms.mean() * 1e3) if len(hit_ms) else None
+    achieved = bytes_hbm / (hit_us * 1e-6) / 1e9 if hit_us else None
+    return {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": (achieved / pk["hbm_gbs"]) if achieved else None, "peak_source": pk["source"],
+            "bytes_per_launch": bytes_hbm, "avg_launch_us": hit_us, "launches": int(len(hit_ms))}
+
+
+def h2d_figures(w, r: dict, h2d_peak) -> dict:
+    """Host-link figures of the missed (or bypassed) expert copies.  Primary:
+    bytes / copy span, where the span runs from the first chunk the staged
+    kernel's copier warps issued to the last one landed, per launch (FUSED copy
+    mode).  Secondary: the slope of MLP-launch time against its miss count."""
+    lay = synth.expert_layout(w.wdtype, w.hidden, w.inter)
+    Be = lay["total"]
+    sp = r["spans"]
+    ok = (sp[:, 2] > 0) & (sp[:, 1] > sp[:, 0]) if len(sp) else np.zeros(0, bool)
+    span_s = float((sp[ok, 1] - sp[ok, 0]).astype(np.float64).sum()) * 1e-9 if ok.any() else 0.0
+    span_bytes = float(sp[ok, 2].astype(np.float64).sum()) * Be if ok.any() else 0.0
+    gbs = span_bytes / span_s / 1e9 if span_s > 0 else None
+    ms, miss = r["mlp_ms"], r["mlp_miss"]
+    base_ms, per_miss_ms = _fit_per_miss(ms[ms > 0], miss[ms > 0]) if len(ms) else (None, None)
+    slope_gbs = Be / (per_miss_ms * 1e-3) / 1e9 if per_miss_ms and per_miss_ms > 0 else None
+    st0, st1 = r["st0"], r["st1"]
+    out = {"miss_gbs": gbs, "peak_gbs": h2d_peak,
+           "frac": (gbs / h2d_peak) if (gbs and h2d_peak) else None,
+           "how": "bytes copied / copy span (first chunk issued to last chunk landed) of the staged kernel's "
+                  "copier warps, summed over the timed launches that copied",
+           "copy_launches": int(ok.sum()), "span_bytes": span_bytes,
+           "span_us_per_launch": (span_s * 1e6 / ok.sum()) if ok.any() else None,
+           "miss_bytes": int(st1["bytes_h2d_miss"] - st0["bytes_h2d_miss"] + st1["bytes_h2d_bypass"]
+                             - st0["bytes_h2d_bypass"]),
+           "slope": {"per_miss_us": per_miss_ms * 1e3 if per_miss_ms else None,
+                     "mlp_base_us": base_ms * 1e3 if base_ms is not None else None,
+                     "gbs": slope_gbs,
+                     "how": "marginal MLP-launch time per miss (least squares); overlap makes it exceed the link"}}
+    if gbs is None and r["tm"]["copy_ms"] > 0:
+        # copy kernel or cudaMemcpyAsync on the copy stream: event time of the copies
+        out["miss_gbs"] = out["miss_bytes"] / (r["tm"]["copy_ms"] * 1e-3) / 1e9
+        out["frac"] = out["miss_gbs"] / h2d_peak if h2d_peak else None
+        out["how"] = "bytes copied / event time of the copy-stream launches"
+    return out
+
+
+def cache_counts(r: dict) -> dict:
+    st0, st1 = r["st0"], r["st1"]
+    d = {k: int(st1[k] - st0[k]) for k in ("hits", "misses", "evictions", "bypass_steps", "cold_reads")}
+    d["hit_rate"] = d["hits"] / max(1, d["hits"] + d["misses"])
+    return d
+
+
+# ---------------------------------------------------------------------------
+# the INT4 pool-size sweep and batched decode
+# ---------------------------------------------------------------------------
+
+def int4_decode(args, dev, world, src, pk) -> dict:
+    """Flash-Next-shaped INT4 decode (batch 1, 16 layers) at N = 0, 16, 32, 64
+    slots per layer, and with every expert resident (N = E)."""
+    from expert_slot_cache_topk_gb300._abi import MoECache
+    base = synth.WORKLOADS["int4"]
     if args.layers:
-        w = w.with_(layers=args.layers)
-    if args.prefill_slots >= 0:
-        w = w.with_(slots=args.prefill_slots)
+        base = base.with_(layers=args.layers)
+    points = []
+    for N in (0, 16, 32, 64, base.experts):
+        w = base.with_(slots=N)
+        c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, w.tokens,
+                     copy_mode="auto", device=dev.index)
+        fill_weights(c, w, src)
+        info = c.info()
+        run = DecodeRun(c, w, dev, warmup=args.int4_warmup, steps=args.int4_steps)
+        r = run.measure(world)
+        c.close()
+        max_sec, toks = aggregate(r["sec"], run.steps * w.tokens, world, dev)
+        cc = cache_counts(r)
+        p = {"slots": N, "value": toks / max_sec, "unit": UNIT, "ms_per_token": 1e3 * max_sec / run.steps,
+             "hit_rate": cc["hit_rate"], "misses_per_token": cc["misses"] / run.steps,
+             "bypass_steps_per_token": cc["bypass_steps"] / run.steps, "copy_mode": info["copy_mode_name"],
+             "roofline": kernel_roofline(w, r, pk),
+             "h2d": h2d_figures(w, r, max(info["memcpy_gbs"], info["uva_gbs"]) or None)}
+        points.append(p)
+    return {"workload": (f"int4-shaped decode: {base.layers} MoE layers x {base.experts} experts, top-{base.top_k}, "
+                         f"hidden {base.hidden}, expert inter {base.inter}, int4 g128 (bf16 scales), batch 1, "
+                         f"routing fresh Zipf({base.zipf_s})"),
+            "warmup_steps": args.int4_warmup, "steps": args.int4_steps,
+            "kernel": "k_mlp_ring (staged-weight expert MLP; copier warps move missed experts)",
+            "points": points}
+
+
+def batched_decode(args, dev, world, src, pk) -> dict:
+    """64 sequences per step on the INT4 shapes: N = 64 (steps whose distinct
+    experts exceed the pool bypass it) and every expert resident (the grouped
+    tensor-core GEMM with no copy in flight)."""
+    from expert_slot_cache_topk_gb300._abi import MoECache
+    base = synth.WORKLOADS["batched"]
+    if args.layers:
+        base = base.with_(layers=args.layers)
+    out = {"workload": (f"batched decode: {base.layers} MoE layers x {base.experts} experts, top-{base.top_k}, "
+                        f"hidden {base.hidden}, expert inter {base.inter}, int4 g128, {base.tokens} sequences per "
+                        f"step from {base.topics} Zipf({base.zipf_s}) topic mixtures"),
+           "warmup_steps": args.batched_warmup, "steps": args.batched_steps, "points": []}
+    for N in (base.slots, base.experts):
+        w = base.with_(slots=N)
+        c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, w.tokens,
+                     copy_mode="auto", device=dev.index)
+        fill_weights(c, w, src)
+        run = DecodeRun(c, w, dev, warmup=args.batched_warmup, steps=args.batched_steps)
+        r = run.measure(world)
+        c.close()
+        max_sec, toks = aggregate(r["sec"], run.steps * w.tokens, world, dev)
+        cc = cache_counts(r)
+        tm = r["tm"]
+        flops = run.steps * w.layers * w.tokens * w.top_k * 2 * 3 * w.hidden * w.inter
+        gemm_s = tm["up_ms"] / 1e3
+        tflops = flops / gemm_s / 1e12 if gemm_s > 0 else None
+        copied = r["st1"]["bytes_h2d_miss"] - r["st0"]["bytes_h2d_miss"] + \
+            r["st1"]["bytes_h2d_bypass"] - r["st0"]["bytes_h2d_bypass"]
+        out["points"].append({
+            "slots": N, "value": toks / max_sec, "unit": UNIT, "ms_per_step": 1e3 * max_sec / run.steps,
+            "bypass_fraction": cc["bypass_steps"] / (run.steps * w.layers), "hit_rate": cc["hit_rate"],
+            "grouped_gemm": {"kernel": "k_moe_gemm (tcgen05: group + up + down + combine)", "bound": "tensor",
+                             "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": (tflops / pk["bf16_tflops"]) if tflops else None,
+                             "ms_per_layer": 1e3 * gemm_s / (run.steps * w.layers),
+                             "note": "event time of the GEMM launches; with copies in flight it includes "
+                                     "waits for experts still crossing the host link"},
+            "copy": {"bytes_per_step": copied / run.steps,
+                     "gbs": copied / (tm["copy_ms"] * 1e-3) / 1e9 if tm["copy_ms"] > 0 else None}})
+    return out
+
+
+# ---------------------------------------------------------------------------
+# prefill chunk (bypass + cold set), then decode on the same cache
+# ---------------------------------------------------------------------------
+
+def _prefill_chunks(c, w, dev, reps: int, warm_chunks: int, world):
+    import torch
+    from expert_slot_cache_topk_gb300._abi import MOE_FWD_RESIDUAL
     T = w.prefill_tokens
-    cold = np.stack([synth.cold_mask(w, l) for l in range(w.layers)])
-    c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, T,
-                 cold_mask=cold, copy_mode="auto", device=dev.index)
-    info = c.info()
-    for l in range(w.layers):
-        synth.fill_layer_blocks(w, l, c.backing_view(l).reshape(-1), info["slot_stride"])
     lg = torch.from_numpy(np.stack([synth.prefill_logits(w, l) for l in range(w.layers)])).to(dev)   # [L, T, E]
     x0 = torch.from_numpy(synth.hidden_states(w, 0, 1, tokens=T)[0].view(np.int16)).to(dev).view(torch.bfloat16)
     ys = torch.empty((w.layers, T, w.hidden), dtype=torch.bfloat16, device=dev)
@@ -316,11 +687,11 @@ def run_prefill(args, dev, world):
             x = ys[l]
 
     with torch.cuda.stream(stream):
-        chunk()                                   # warm-up (a bypass chunk leaves the pool as it is)
+        for _ in range(warm_chunks):
+            chunk()
     stream.synchronize()
     st0 = c.stats(-1)
-    c.set_timing(True, capacity=4 * w.layers + 8)
-    reps = 2
+    c.set_timing(True, capacity=4 * w.layers * reps + 8)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -334,16 +705,34 @@ def run_prefill(args, dev, world):
     tm = c.read_timing()
     c.set_timing(False)
     st1 = c.stats(-1)
+    return sec, tm, st0, st1, stream
+
+
+def run_prefill(args, dev, world, src, pk):
+    """Prefill chunk of the prefill + cold-set workload: all layers of one
+    2048-token chunk through moe_forward (the bypass path: every non-cold
+    expert of the chunk is copied to scratch, cold experts are read in place,
+    the grouped expert MLP runs on the tensor cores)."""
+    from expert_slot_cache_topk_gb300._abi import MoECache
+    w = synth.WORKLOADS["prefill_cold"]
+    if args.layers:
+        w = w.with_(layers=args.layers)
+    if args.prefill_slots >= 0:
+        w = w.with_(slots=args.prefill_slots)
+    T = w.prefill_tokens
+    cold = np.stack([synth.cold_mask(w, l) for l in range(w.layers)])
+    c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, T,
+                 cold_mask=cold, copy_mode="auto", device=dev.index)
+    fill_weights(c, w, src)
+    reps = 2
+    sec, tm, st0, st1, stream = _prefill_chunks(c, w, dev, reps, 1, world)
     dec = decode_after_prefill(c, w, dev, stream, world)
     c.close()
     max_sec, all_tok = aggregate(sec, reps * T, world, dev)
-    lay = synth.expert_layout(w.wdtype, w.hidden, w.inter)
-    # dense work of the expert MLP: 2 flops per multiply-add, 3 matrices of H x I per assignment
     flops = reps * w.layers * T * w.top_k * 2 * 3 * w.hidden * w.inter
     gemm_s = tm["up_ms"] / 1e3
     copy_s = tm["copy_ms"] / 1e3
     byp = st1["bytes_h2d_bypass"] - st0["bytes_h2d_bypass"]
-    pk = peaks()
     tflops = flops / gemm_s / 1e12 if gemm_s > 0 else None
     return {
         "workload": (f"prefill chunk: {w.layers} MoE layers x {w.experts} experts, top-{w.top_k}, hidden {w.hidden}, "
@@ -355,65 +744,33 @@ def run_prefill(args, dev, world):
                          "bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": (tflops / pk["bf16_tflops"]) if tflops else None,
                          "flops_per_chunk": flops // reps, "ms_per_chunk": 1e3 * gemm_s / reps,
-                         "note": "INT4 weights are dequantised to bf16 on the CUDA cores while being staged"},
+                         "note": "event time of the GEMM launches, which overlap the bypass copy and wait for "
+                                 "experts still crossing the host link"},
         "bypass_copy": {"bytes_per_chunk": byp // reps, "ms_per_chunk": 1e3 * copy_s / reps,
                         "gbs": byp / copy_s / 1e9 if copy_s > 0 else None},
         "cold_reads_per_chunk": (st1["cold_reads"] - st0["cold_reads"]) // reps,
         "decode_after_prefill": dec,
-        "grouped_gemm_resident": gemm_resident(args, dev, world),
+        "grouped_gemm_resident": gemm_resident(args, dev, world, src, pk),
     }
 
 
-def gemm_resident(args, dev, world, layers=4):
+def gemm_resident(args, dev, world, src, pk, layers=4):
     """The grouped GEMM alone: a prefill chunk on a few layers whose pools hold
     every non-cold expert (N = E - cold), after a first chunk has filled them,
     so no copy is in flight while the tensor cores run."""
-    import torch
-    from expert_slot_cache_topk_gb300._abi import MOE_FWD_RESIDUAL, MoECache
+    from expert_slot_cache_topk_gb300._abi import MoECache
     w = synth.WORKLOADS["prefill_cold"]
     w = w.with_(layers=min(layers, args.layers or layers), slots=w.experts - w.n_cold)
     T = w.prefill_tokens
     cold = np.stack([synth.cold_mask(w, l) for l in range(w.layers)])
     c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, T,
                  cold_mask=cold, copy_mode="auto", device=dev.index)
-    info = c.info()
-    for l in range(w.layers):
-        synth.fill_layer_blocks(w, l, c.backing_view(l).reshape(-1), info["slot_stride"])
-    lg = torch.from_numpy(np.stack([synth.prefill_logits(w, l) for l in range(w.layers)])).to(dev)
-    x0 = torch.from_numpy(synth.hidden_states(w, 0, 1, tokens=T)[0].view(np.int16)).to(dev).view(torch.bfloat16)
-    ys = torch.empty((w.layers, T, w.hidden), dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.Stream(dev)
-
-    def chunk():
-        x = x0
-        for l in range(w.layers):
-            c.forward(l, x, lg[l], T, ys[l], MOE_FWD_RESIDUAL, stream)
-            x = ys[l]
-
-    with torch.cuda.stream(stream):
-        chunk()                       # fills the pools (every non-cold expert misses once)
-        chunk()
-    stream.synchronize()
-    st0 = c.stats(-1)
-    c.set_timing(True, capacity=4 * w.layers + 8)
+    fill_weights(c, w, src)
     reps = 2
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(reps):
-            chunk()
-        ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    sec = ev0.elapsed_time(ev1) / 1e3
-    tm = c.read_timing()
-    c.set_timing(False)
-    st1 = c.stats(-1)
+    sec, tm, st0, st1, _ = _prefill_chunks(c, w, dev, reps, 2, world)
     c.close()
     flops = reps * w.layers * T * w.top_k * 2 * 3 * w.hidden * w.inter
     gemm_s = tm["up_ms"] / 1e3
-    pk = peaks()
     tflops = flops / gemm_s / 1e12 if gemm_s > 0 else None
     max_sec, all_tok = aggregate(sec, reps * T, world, dev)
     return {"layers": w.layers, "slots": w.slots, "value": all_tok / max_sec, "unit": "tok/s",
@@ -476,10 +833,14 @@ def decode_after_prefill(c, w, dev, stream, world, warmup=32, steps=128):
             "hit_rate": hits / max(1, hits + misses), "warm_misses": st0["misses"] - st_w["misses"]}
 
 
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
 def run_ours(args, w):
     import torch
     from expert_slot_cache_topk_gb300 import _build
-    from expert_slot_cache_topk_gb300._abi import MOE_FWD_RESIDUAL, MoECache
+    from expert_slot_cache_topk_gb300._abi import MoECache
 
     rank, local_rank, world = dist_env()
     torch.cuda.set_device(local_rank)
@@ -488,205 +849,104 @@ def run_ours(args, w):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     _build.build()
+    pk = peaks()
 
-    S = args.warmup + args.steps
     c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, w.tokens,
                  copy_mode=args.copy_mode, device=local_rank, table=args.table)
     info = c.info()
     t0 = time.time()
-    for l in range(w.layers):
-        synth.fill_layer_blocks(w, l, c.backing_view(l).reshape(-1), info["slot_stride"])
+    fill_weights(c, w)
     fill_s = time.time() - t0
-    lg = np.stack([synth.routing_logits(w, l, S) for l in range(w.layers)], axis=1)   # [S, L, T, E]
-    x0 = synth.hidden_states(w, 0, S)                                                 # [S, T, H]
-    lg_d = torch.from_numpy(lg).to(dev)
-    x0_d = torch.from_numpy(x0.view(np.int16)).to(dev).view(torch.bfloat16)
-    # every step has its own output buffers, so a graph of all timed steps needs no copies
-    ys = torch.empty((S, w.layers, w.tokens, w.hidden), dtype=torch.bfloat16, device=dev)
+    run = DecodeRun(c, w, dev, warmup=args.warmup, steps=args.steps, graph=not args.no_graph)
+    r = run.measure(world, args.clock_ms, local_rank)
 
-    def step(s, stream):
-        x = x0_d[s]
-        for l in range(w.layers):
-            c.forward(l, x, lg_d[s, l], w.tokens, ys[s, l], MOE_FWD_RESIDUAL, stream)
-            x = ys[s, l]
-
-    stream = torch.cuda.Stream(dev)
-    torch.cuda.current_stream(dev).synchronize()
-    # MEMCPY mode takes a host decision per layer step, so it cannot be captured
-    use_graph = not args.no_graph and info["copy_mode_name"] != "memcpy"
-
-    def warm():
-        c.reset()
-        with torch.cuda.stream(stream):
-            for s in range(args.warmup):
-                step(s, stream)
-        stream.synchronize()
-
-    def prime(timing: bool):
-        """Empty the pools, run the warm-up steps, then capture (or not) the timed
-        steps; returns (graph or None, kernel launches of the timed steps).  The
-        uninstrumented graph is replayed once untimed (its first launch uploads
-        it to the device), then the pools are emptied and warmed up again, so
-        that the timed replay starts from the state the capture saw."""
-        warm()
-        c.set_timing(timing, capacity=args.steps * w.layers + 64)
-        l0 = c.info()["kernel_launches"]
-        g = None
-        if use_graph:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                with torch.cuda.graph(g, stream=stream):
-                    for s in range(args.warmup, S):
-                        step(s, stream)
-            stream.synchronize()
-            n = c.info()["kernel_launches"] - l0
-            if not timing:
-                with torch.cuda.stream(stream):
-                    g.replay()
-                stream.synchronize()
-                warm()
-            return g, n
-        return g, c.info()["kernel_launches"] - l0
-
-    def timed(g, sampler_ms):
-        """Run the timed steps once; (seconds, kernel launches, clock summary)."""
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        l0 = c.info()["kernel_launches"]
-        clk = ClockSampler(local_rank, sampler_ms)
-        with (clk if sampler_ms > 0 else contextlib.nullcontext()):
-            barrier(world)
-            torch.cuda.synchronize(dev)
-            with torch.cuda.stream(stream):
-                ev0.record(stream)
-                if g is not None:
-                    g.replay()
-                else:
-                    for s in range(args.warmup, S):
-                        step(s, stream)
-                ev1.record(stream)
-            torch.cuda.synchronize(dev)
-            barrier(world)
-        return (ev0.elapsed_time(ev1) / 1e3, c.info()["kernel_launches"] - l0,
-                clk.summary() if sampler_ms > 0 else None)
-
-    # (1) the headline: the timed steps with no instrumentation
-    graph, launches = prime(False)
-    st0 = c.stats(-1)
-    sec, eager_launches, clocks = timed(graph, args.clock_ms)
-    if graph is None:
-        launches = eager_launches
-    st1 = c.stats(-1)
-    del graph
-    # (1b) cold start: every step from an empty pool (warm-up steps included),
+    # cold start: every step from an empty pool (warm-up steps included),
     # replayed from a graph uploaded by one untimed replay
     cold_sec = None
-    if use_graph:
+    if run.use_graph:
+        S = args.warmup + args.steps
         c.reset()
         gc = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(gc, stream=stream):
+        with torch.cuda.stream(run.stream):
+            with torch.cuda.graph(gc, stream=run.stream):
                 for s in range(S):
-                    step(s, stream)
+                    run.step(s)
             gc.replay()
-        stream.synchronize()
+        run.stream.synchronize()
         c.reset()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
+        with torch.cuda.stream(run.stream):
+            e0.record(run.stream)
             gc.replay()
-            e1.record(stream)
+            e1.record(run.stream)
         torch.cuda.synchronize(dev)
         cold_sec = e0.elapsed_time(e1) / 1e3
         del gc
-    # (2) the same steps from the same state again, with per-launch events and
-    # miss counts, for the kernel roofline and the per-miss fit
-    graph_t, _ = prime(True)
-    timed(graph_t, 0)
-    del graph_t
-    tm = c.read_timing()
-    mlp_ms, mlp_miss = c.read_timing_launches()
-    c.set_timing(False)
-    tokens = args.steps * w.tokens
-    max_sec, all_tokens = aggregate(sec, tokens, world, dev)
 
-    # roofline of the expert-MLP kernel over the launches with no miss: every
-    # byte of the k experts' blocks is read from HBM once per launch
-    lay = synth.expert_layout(w.wdtype, w.hidden, w.inter)
-    bytes_hbm = w.tokens * w.top_k * lay["total"]
-    pk = peaks()
-    hit_ms = mlp_ms[(mlp_miss == 0) & (mlp_ms > 0)]
-    hit_us = float(hit_ms.mean() * 1e3) if len(hit_ms) else None
-    achieved = bytes_hbm / (hit_us * 1e-6) / 1e9 if hit_us else None
-    base_ms, per_miss_ms = _fit_per_miss(mlp_ms[mlp_ms > 0], mlp_miss[mlp_ms > 0])
-    miss_gbs = lay["total"] / (per_miss_ms * 1e-3) / 1e9 if per_miss_ms and per_miss_ms > 0 else None
-    miss_bytes = st1["bytes_h2d_miss"] - st0["bytes_h2d_miss"] + st1["bytes_h2d_bypass"] - st0["bytes_h2d_bypass"]
+    tokens = args.steps * w.tokens
+    max_sec, all_tokens = aggregate(r["sec"], tokens, world, dev)
+    roof = kernel_roofline(w, r, pk)
+    roof["kernel"] = "k_mlp_ring (staged-weight expert MLP: w13 + SiLU-mul + w2, launches with no miss)"
+    roof["traffic"] = MEASURED_TRAFFIC.get((w.name, kernel_source_tag()))
     h2d_peak = max(info["memcpy_gbs"], info["uva_gbs"]) or None
+    h2d = h2d_figures(w, r, h2d_peak)
+    ms, miss = r["mlp_ms"], r["mlp_miss"]
+    h2d["mlp_us_by_misses"] = {str(m): float(ms[(miss == m) & (ms > 0)].mean() * 1e3)
+                               for m in range(4) if ((miss == m) & (ms > 0)).any()}
 
     # end-to-end through the C ABI with host buffers (copies inside the timed
     # region): the same warm-up, then the first timed steps
     e2e_steps = min(args.e2e_steps, args.steps)
-    x_h = torch.from_numpy(x0.view(np.int16).copy()).pin_memory().numpy()
-    lg_h = torch.from_numpy(np.ascontiguousarray(lg)).pin_memory().numpy()
+    x_h = torch.from_numpy(run.x0.view(np.int16).copy()).pin_memory().numpy()
+    lg_h = torch.from_numpy(np.ascontiguousarray(run.lg)).pin_memory().numpy()
     y_h = torch.empty((w.tokens, w.hidden), dtype=torch.int16).pin_memory().numpy()
     c.reset()
     for s in range(args.warmup):
-        c.model_step_host(x_h[s], lg_h[s], w.tokens, y_h, 60000, stream)
+        c.model_step_host(x_h[s], lg_h[s], w.tokens, y_h, 60000, run.stream)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for s in range(args.warmup, args.warmup + e2e_steps):
-        c.model_step_host(x_h[s], lg_h[s], w.tokens, y_h, 60000, stream)
+        c.model_step_host(x_h[s], lg_h[s], w.tokens, y_h, 60000, run.stream)
     e2e_s = time.perf_counter() - t0
     e2e_sec, e2e_tok = aggregate(e2e_s, e2e_steps * w.tokens, world, dev)
-
-    if rank == 0:
-        cpu_v, cpu_n, cpu_dt = (None, 0, 0.0)
-        if world == 1 and not args.no_cpu_baseline:
-            cpu_v, cpu_n, cpu_dt = oracle_tokens_per_s(w, 2, budget_s=args.cpu_budget)
-        line = {
-            "metric": METRIC, "value": all_tokens / max_sec, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * max_sec / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.wdtype],
-            "data": "synthetic (seeded Zipf routing with reuse; N(0,0.02) weights)",
-            "config": {"workload": workload_desc(w), "tokens_per_step": w.tokens,
-                       "copy_mode": info["copy_mode_name"], "graph": use_graph, "table": args.table,
-                       "l2": "inputs larger than L2: every step reads "
-                             f"{w.layers * w.top_k * lay['total'] / 1e9:.2f} GB of expert weights",
-                       "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "k_mlp_ring (staged-weight expert MLP: w13 + SiLU-mul + w2, launches with no miss)",
-                         "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
-                         "traffic": MEASURED_TRAFFIC.get((w.name, kernel_source_tag())),
-                         "peak_source": pk["source"], "bytes_per_launch": bytes_hbm,
-                         "avg_launch_us": hit_us, "launches": int(len(hit_ms))},
-            "h2d": {"miss_bytes": miss_bytes, "miss_gbs": miss_gbs,
-                    "per_miss_us": per_miss_ms * 1e3 if per_miss_ms else None,
-                    "mlp_base_us": base_ms * 1e3 if base_ms is not None else None,
-                    "peak_gbs": h2d_peak, "frac": (miss_gbs / h2d_peak) if (miss_gbs and h2d_peak) else None,
-                    "how": "slope of MLP-launch time vs misses in that layer step (least squares)",
-                    "mlp_us_by_misses": {str(m): float(mlp_ms[(mlp_miss == m) & (mlp_ms > 0)].mean() * 1e3)
-                                         for m in range(4) if ((mlp_miss == m) & (mlp_ms > 0)).any()}},
-            "phases_ms_per_step": {k[:-3]: tm[k] / args.steps for k in ("route_ms", "copy_ms", "up_ms", "down_ms")},
-            "cache": dict({k: st1[k] - st0[k] for k in ("hits", "misses", "evictions", "bypass_steps")},
-                          hit_rate=(st1["hits"] - st0["hits"]) / max(1, st1["hits"] - st0["hits"] + st1["misses"] - st0["misses"])),
-            "cold_start": ({"value": S * w.tokens / cold_sec, "unit": UNIT, "steps": S,
-                            "note": "all steps from an empty pool, warm-up steps included"}
-                           if cold_sec else None),
-            "e2e": {"value": (e2e_tok / e2e_sec) if e2e_steps > 0 else None, "unit": UNIT,
-                    "h2d_bytes_per_step": int(x_h[0].nbytes + lg_h[0].nbytes),
-                    "d2h_bytes_per_step": int(y_h.nbytes)},
-            "gpu_launches": int(launches),
-            "clocks": clocks,
-            "setup_s": {"fill_weights": fill_s},
-        }
-        if cpu_v is not None:
-            line["cpu_baseline"] = {"value": cpu_v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                                    "sample": f"{cpu_n} (token, layer) steps of the first 2 decode tokens "
-                                              f"in {cpu_dt:.1f} s (float64 numpy, BLAS threads as installed)"}
     c.close()
-    prefill = None if args.no_prefill else run_prefill(args, dev, world)
+    del run
+
+    line = {
+        "metric": METRIC, "value": all_tokens / max_sec, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * max_sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.wdtype],
+        "data": DATA, "config": run_config(w, world),
+        "engine": {"copy_mode": info["copy_mode_name"], "graph": not args.no_graph, "table": args.table},
+        "roofline": roof,
+        "h2d": h2d,
+        "phases_ms_per_step": {k[:-3]: r["tm"][k] / args.steps for k in ("route_ms", "copy_ms", "up_ms", "down_ms")},
+        "cache": cache_counts(r),
+        "cold_start": ({"value": (args.warmup + args.steps) * w.tokens / cold_sec, "unit": UNIT,
+                        "steps": args.warmup + args.steps,
+                        "note": "all steps from an empty pool, warm-up steps included"} if cold_sec else None),
+        "e2e": {"value": (e2e_tok / e2e_sec) if e2e_steps > 0 else None, "unit": UNIT,
+                "h2d_bytes_per_step": int(x_h[0].nbytes + lg_h[0].nbytes),
+                "d2h_bytes_per_step": int(y_h.nbytes)},
+        "gpu_launches": int(r["launches"]),
+        "clocks": r["clocks"],
+        "setup_s": {"fill_weights": fill_s},
+    }
+    # the other workloads of the path (INT4 weights generated once, shared)
+    src = Int4Weights()
+    if not args.no_int4:
+        line["int4_decode"] = int4_decode(args, dev, world, src, pk)
+    if not args.no_batched:
+        line["batched_decode"] = batched_decode(args, dev, world, src, pk)
+    if not args.no_prefill:
+        line["prefill"] = run_prefill(args, dev, world, src, pk)
+    line["setup_s"]["int4_weights"] = src.gen_s
+    if (line.get("int4_decode") or line.get("batched_decode") or line.get("prefill")) and src.layers:
+        line["setup_s"]["int4_note"] = ("the INT4 workloads (sweep, batched, prefill) share the int4 workload's "
+                                        "generated expert weights; routing is each workload's own")
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     if rank == 0:
-        if prefill is not None:
-            line["prefill"] = prefill
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -710,12 +970,22 @@ def main():
                     help="override the decode workload's weight format")
     ap.add_argument("--clock-ms", type=int, default=100, help="nvidia-smi sampling interval in ms")
     ap.add_argument("--e2e-steps", type=int, default=64)
-    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--int4-steps", type=int, default=128, help="timed steps per INT4 pool size")
+    ap.add_argument("--int4-warmup", type=int, default=32)
+    ap.add_argument("--batched-steps", type=int, default=16, help="timed 64-token steps of batched decode")
+    ap.add_argument("--batched-warmup", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-chunk measurement")
+    ap.add_argument("--no-int4", action="store_true", help="skip the INT4 pool-size sweep")
+    ap.add_argument("--no-batched", action="store_true", help="skip batched decode")
     ap.add_argument("--prefill-slots", type=int, default=-1, help="pool slots per layer for the prefill chunk")
+    ap.add_argument("--oracle-child", default="", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_child:
+        oracle_child(args.oracle_child, args.cpu_budget)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = synth.WORKLOADS[args.workload]

@@ -107,6 +107,7 @@ SIGNATURES = {
     "moe_cache_set_timing": (_S, [_H, _I, _I]),
     "moe_cache_read_timing": (_S, [_H, C.POINTER(moe_cache_timing)]),
     "moe_cache_read_timing_launches": (_S, [_H, _P, _P, _I, C.POINTER(_I)]),
+    "moe_cache_read_copy_spans": (_S, [_H, _P, _I, C.POINTER(_I)]),
 }
 
 _lib = None
@@ -341,6 +342,13 @@ class MoECache:
         self._ck(lib().moe_cache_read_timing_launches(self._h, ms.ctypes.data, mi.ctypes.data, cap,
                                                       C.byref(n)))
         return ms[: n.value], mi[: n.value]
+
+    def read_copy_spans(self, cap: int = 1 << 16):
+        """Per timed MLP launch: (first chunk issued ns, last chunk landed ns, experts copied), uint64 [n, 3]."""
+        rec = np.zeros((cap, 3), np.uint64)
+        n = C.c_int()
+        self._ck(lib().moe_cache_read_copy_spans(self._h, rec.ctypes.data, cap, C.byref(n)))
+        return rec[: n.value]
 
     def read_timing(self) -> dict:
         t = moe_cache_timing()

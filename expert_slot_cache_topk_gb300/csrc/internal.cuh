@@ -72,7 +72,7 @@ struct PrepArgs {
   int32_t* slot_expert;              // [N]
   long long* slot_stamp;             // [N]
   int32_t* slot_aux;                 // [N]: LFU steps used, SLRU segment (1 = protected)
-  unsigned* ring_cnt;                // [2 * MOE_MAX_TOPK] or null: zeroed (copy counts of the next MLP)
+  unsigned* ring_cnt;                // [3 * MOE_MAX_TOPK] or null: zeroed (copy and h counts of the next MLP)
   int policy;                        // moe_evict_policy
   LayerState* st;
   RecHdr* hdr;
@@ -133,7 +133,18 @@ struct MlpArgs {
   // the staged decode kernel reads blocks there with plain loads, never with
   // bulk copies (0, 0 = no host blocks).
   unsigned long long host_lo, host_hi;
+  // Timing only (null otherwise): the staged kernel's copier writes, every
+  // launch and without atomics, copy_span[0] = blocks copied, copy_span[1] =
+  // grid size, and per CTA b copy_span[2 + 2b] / [3 + 2b] = global time its
+  // copier warp issued its first chunk / had landed its last one (0, 0 when it
+  // copied nothing).  Launches with more than kSpanMaxCtas CTAs record nothing.
+  unsigned long long* copy_span;
+  // Staged decode kernel: h_cnt[j] counts the gate/up pairs of assignment j
+  // whose h is written (zeroed by prepare); null = the kernel is not used.
+  unsigned* h_cnt;
 };
+constexpr int kSpanMaxCtas = 256;
+constexpr int kSpanRecWords = 2 + 2 * kSpanMaxCtas;   // u64 words of one launch's copy-span record
 
 // ---- launchers (k_route_prepare.cu) ----
 cudaError_t launch_router(const float* logits, int T, int E, int k, int renorm,
@@ -183,6 +194,7 @@ size_t mlp_up_smem_bytes(int H);
 
 // ---- launchers (k_mlp_ring.cu): one-token expert MLP with weights staged in
 // shared memory by bulk copies; cudaErrorNotSupported = use launch_mlp_fused.
+// `bar` is not used by this kernel (its CTAs wait on per-expert h counts).
 cudaError_t mlp_ring_configure(int wdtype, int H, int I, int k);  // call outside capture
 cudaError_t launch_mlp_ring(int wdtype, const MlpArgs& a, GridBar* bar, int* err, cudaStream_t s);
 // floats the staged kernel's h scratch needs (it keeps several copies of h)

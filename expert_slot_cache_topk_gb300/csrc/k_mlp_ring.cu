@@ -260,16 +260,153 @@ struct RingTile<MOE_FP8_E4M3> {
   static constexpr int XM = 4, HM = 4;
 };
 
-// dot product of one 16-byte weight chunk with EL activations in registers
+// ---- activations in registers
+// bf16 / f32 / FP8: a chunk's EL activations as f32.  INT4: a chunk of 32
+// activations as 16-bit integers at a power-of-two scale (Q4Act below), so that
+// a 16-byte chunk of packed codes is dotted in exact integer arithmetic.
+template <int EL>
+struct FAct {
+  float v[EL];
+};
+
+// INT4 activation chunk.  With s chosen so that the chunk's largest magnitude
+// times 2^s lies in [2^13, 2^14): even elements X = rint(x 2^s) (|X| <= 2^14),
+// odd elements Y = rint(x 2^(s-4)) (|Y| <= 2^10), i.e. the odd element's
+// integer is 16 Y.  A 32-bit weight word holds the codes of elements 8k .. 8k+7,
+// byte i = q[2i] + 16 q[2i+1] (low nibble = even column).  dp2a (two 16-bit x
+// 8-bit products per instruction) of the raw bytes with (Y_{2i+1}) pairs gives
+// Y q_even + 16 Y q_odd, and of the even codes (word & 0x0F0F0F0F) with
+// (X_{2i} - Y_{2i+1}) pairs completes X q_even: four dp2a and one LOP3 per word
+// give sum q X over its eight elements.  The offset of the codes enters as the
+// starting value -8 sum X, so the chunk's D = sum (q - 8) X is exact in int32
+// (|D| <= 2^22, exact in f32 too), and the chunk's dot is D * 2^-s.  Activations
+// keep 14 significant bits (even) and 10 (odd) relative to the chunk's largest,
+// i.e. every bf16 x at least 1/4 of the chunk's largest is exact.
+struct Q4Act {
+  uint32_t p[16];   // word k: (Y1,Y3), (Y5,Y7), (X0-Y1, X2-Y3), (X4-Y5, X6-Y7) of elements 8k + i
+  int off;          // -8 * sum of the 32 integers
+  float sc;         // 2^-s (NaN when the chunk holds a NaN or an infinity)
+};
+
 template <int F>
-__device__ __forceinline__ float chunk_dot_r(const uint4 w, const float* x) {
-  return chunk_dot<F>(w, x);
+struct ActSel {
+  using type = FAct<FmtT<F>::kElems>;
+};
+template <>
+struct ActSel<MOE_INT4_G128> {
+  using type = Q4Act;
+};
+template <int F>
+using ActT = typename ActSel<F>::type;
+
+__device__ __forceinline__ uint32_t pack_s16x2(int lo, int hi) {
+  return ((uint32_t)lo & 0xffffu) | ((uint32_t)hi << 16);
+}
+
+// 32 activations (f32) -> Q4Act
+__device__ __forceinline__ void q4_pack(const float (&x)[32], Q4Act& a) {
+  float mx = 0.f;
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float v = fabsf(x[i]);
+    finite = finite && v <= 3.402823466e38f;   // false for NaN and infinities
+    mx = fmaxf(mx, v);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a.p[i] = 0u;
+  a.off = 0;
+  a.sc = 1.f;
+  if (!finite) {
+    a.sc = __int_as_float(0x7fc00000);   // the chunk's dot becomes NaN, as in float arithmetic
+    return;
+  }
+  if (mx < 5.421010862e-20f) return;      // below 2^-64: contributes nothing measurable
+  const int e = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127;   // mx normal here
+  const int sh = 13 - e;                                            // in [-114, 77]
+  const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
+  const float up16 = __uint_as_float((uint32_t)(127 + sh - 4) << 23);
+  a.sc = __uint_as_float((uint32_t)(127 - sh) << 23);
+  int sum = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float* xk = x + 8 * k;
+    const int X0 = __float2int_rn(xk[0] * up), X2 = __float2int_rn(xk[2] * up);
+    const int X4 = __float2int_rn(xk[4] * up), X6 = __float2int_rn(xk[6] * up);
+    const int Y1 = __float2int_rn(xk[1] * up16), Y3 = __float2int_rn(xk[3] * up16);
+    const int Y5 = __float2int_rn(xk[5] * up16), Y7 = __float2int_rn(xk[7] * up16);
+    sum += X0 + X2 + X4 + X6 + 16 * (Y1 + Y3 + Y5 + Y7);
+    a.p[4 * k + 0] = pack_s16x2(Y1, Y3);
+    a.p[4 * k + 1] = pack_s16x2(Y5, Y7);
+    a.p[4 * k + 2] = pack_s16x2(X0 - Y1, X2 - Y3);
+    a.p[4 * k + 3] = pack_s16x2(X4 - Y5, X6 - Y7);
+  }
+  a.off = -8 * sum;
+}
+
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// sum over the chunk of (q - 8) X, exact
+__device__ __forceinline__ int q4_dot(const uint4 w, const Q4Act& a) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  int d = a.off;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t ev = ws[k] & 0x0F0F0F0Fu;
+    d = dp2a_lo(a.p[4 * k + 0], ws[k], d);
+    d = dp2a_hi(a.p[4 * k + 1], ws[k], d);
+    d = dp2a_lo(a.p[4 * k + 2], ev, d);
+    d = dp2a_hi(a.p[4 * k + 3], ev, d);
+  }
+  return d;
+}
+
+// dot product of one 16-byte weight chunk with a chunk of activations in
+// registers (INT4: before the group scale, which the caller applies)
+template <int F>
+__device__ __forceinline__ float chunk_dot_r(const uint4 w, const ActT<F>& x) {
+  if constexpr (F == MOE_INT4_G128) return (float)q4_dot(w, x) * x.sc;
+  else return chunk_dot<F>(w, x.v);
+}
+
+// an all-zero activation chunk (past the end of x or of this warp's part of h)
+template <int F>
+__device__ __forceinline__ void act_zero(ActT<F>& a) {
+  if constexpr (F == MOE_INT4_G128) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a.p[i] = 0u;
+    a.off = 0;
+    a.sc = 1.f;
+  } else {
+#pragma unroll
+    for (int e = 0; e < FmtT<F>::kElems; ++e) a.v[e] = 0.f;
+  }
+}
+
+// EL activations as f32 -> the register form
+template <int F>
+__device__ __forceinline__ void act_set(ActT<F>& a, const float (&v)[FmtT<F>::kElems]) {
+  if constexpr (F == MOE_INT4_G128) q4_pack(v, a);
+  else {
+#pragma unroll
+    for (int e = 0; e < FmtT<F>::kElems; ++e) a.v[e] = v[e];
+  }
 }
 
 // activation chunk (EL values) -> registers; x is bf16 unless F is f32
 template <int F>
-__device__ __forceinline__ void load_x_chunk(float* dst, const void* x, int c) {
+__device__ __forceinline__ void load_x_chunk(ActT<F>& act, const void* x, int c) {
   constexpr int EL = FmtT<F>::kElems;
+  float dst[EL];
   if (F == MOE_F32) {
     const float4 v = reinterpret_cast<const float4*>(x)[c];
     dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
@@ -282,6 +419,7 @@ __device__ __forceinline__ void load_x_chunk(float* dst, const void* x, int c) {
       d[4] = bf16_lo(v.z); d[5] = bf16_hi(v.z); d[6] = bf16_lo(v.w); d[7] = bf16_hi(v.w);
     }
   }
+  act_set<F>(act, dst);
 }
 
 // Dot products of NR weight rows with the token's x (registers), reduced
@@ -292,7 +430,7 @@ __device__ __forceinline__ void load_x_chunk(float* dst, const void* x, int c) {
 template <int F, int NR>
 __device__ __forceinline__ void rows_dot(const uint4* const (&row)[NR], const uint16_t* const (&srow)[NR],
                                          uint4* const (&cpy)[NR], bool ring, bool copy, int C,
-                                         const float (&xr)[RingTile<F>::XM][FmtT<F>::kElems], int lane,
+                                         const ActT<F> (&xr)[RingTile<F>::XM], int lane,
                                          float (&out)[NR]) {
   constexpr int XM = RingTile<F>::XM;
   uint4 wv[NR][XM];
@@ -367,7 +505,7 @@ __device__ __forceinline__ float swiglu_h(const RingShared& S, unsigned long lon
 //   writes h), so no barrier is needed.
 template <int F>
 __device__ __forceinline__ void up_item(const MlpArgs& a, RingShared& S, const RingDesc& d, int s,
-                                        const uint8_t* stage, const float (&xr)[RingTile<F>::XM][FmtT<F>::kElems],
+                                        const uint8_t* stage, const ActT<F> (&xr)[RingTile<F>::XM],
                                         int cw, int lane) {
   const int P = d.n;
   const int C = a.H / FmtT<F>::kElems;
@@ -430,7 +568,7 @@ __device__ __forceinline__ void up_item(const MlpArgs& a, RingShared& S, const R
 // expert row) of this lane's chunk m, or -1.
 template <int F>
 __device__ __forceinline__ void down_rows(const MlpArgs& a, const RingShared& S, const RingDesc& d,
-                                          const uint8_t* stage, const float (&hr)[RingTile<F>::HM][FmtT<F>::kElems],
+                                          const uint8_t* stage, const ActT<F> (&hr)[RingTile<F>::HM],
                                           const int (&qj)[RingTile<F>::HM], float* part, int cw, int lane) {
   constexpr int HM = RingTile<F>::HM;
   const int G2 = a.I / 128;
@@ -577,10 +715,22 @@ __device__ __forceinline__ void copier(const MlpArgs& a, const RingShared& S, in
   const unsigned long long b = lane < a.k ? S.base[lane] : 0ull;
   const unsigned pend = __ballot_sync(
       kFull, lane < a.k && a.pending[lane] != 0 && b != 0ull && !in_host(a, b) && (b & 15ull) == 0ull);
-  if (pend == 0u) return;
   const long long np = __popc(pend);
+  // timing record (see MlpArgs::copy_span): header, then this CTA's span
+  unsigned long long* rec = (a.copy_span != nullptr && gridDim.x <= (unsigned)kSpanMaxCtas)
+                                ? a.copy_span + 2 + 2 * (size_t)blockIdx.x : nullptr;
+  if (rec != nullptr && blockIdx.x == 0 && lane == 0) {
+    a.copy_span[0] = (unsigned long long)np;
+    a.copy_span[1] = gridDim.x;
+  }
+  if (pend == 0u) {
+    if (rec != nullptr && lane == 0) rec[0] = rec[1] = 0ull;
+    return;
+  }
   const int nA = phase_chunks(a, false), nB = phase_chunks(a, true);
   const long long total = np * (nA + nB);
+  // timing: when this warp issued its first chunk (warp-uniform)
+  const unsigned long long t_first = (rec != nullptr && blockIdx.x < total) ? global_ns() : 0ull;
   for (long long ci = blockIdx.x; ci < total; ci += gridDim.x) {
     const bool pb = ci >= np * nA;
     const long long cc = pb ? ci - np * nA : ci;
@@ -611,6 +761,11 @@ __device__ __forceinline__ void copier(const MlpArgs& a, const RingShared& S, in
       if (!pb) red_release_add(a.copy_cnt + j, 1u);
       red_release_add(a.copy_cnt + MOE_MAX_TOPK + j, 1u);
     }
+  }
+  if (rec != nullptr && lane == 0) {
+    // every chunk of this warp has landed (fenced above)
+    rec[0] = t_first;
+    rec[1] = blockIdx.x < total ? global_ns() : 0ull;
   }
 }
 
@@ -835,17 +990,13 @@ __device__ __forceinline__ void consume(const MlpArgs& a, const RingCfg& rc, Rin
   int i = 0;
   // ---- up items: x of the token in registers
   {
-    float xr[XM][EL];
+    ActT<F> xr[XM];
     const int C = a.H / EL;
 #pragma unroll
     for (int m = 0; m < XM; ++m) {
       const int c = lane + 32 * m;
-      if (c < C) {
-        load_x_chunk<F>(xr[m], a.x, c);
-      } else {
-#pragma unroll
-        for (int e = 0; e < EL; ++e) xr[m][e] = 0.f;
-      }
+      if (c < C) load_x_chunk<F>(xr[m], a.x, c);
+      else act_zero<F>(xr[m]);
     }
     for (; i < w.n_up; ++i) {
       const int s = i % NS;
@@ -880,28 +1031,30 @@ __device__ __forceinline__ void consume(const MlpArgs& a, const RingCfg& rc, Rin
     const int q_end = min(Q, (pt + 1) * Qp);
     // this warp's part of h (k * I f32, written by every CTA) -> registers,
     // straight from L2
-    float hr[HM][EL];
+    ActT<F> hr[HM];
     int qj[HM];
 #pragma unroll
     for (int m = 0; m < HM; ++m) {
       const int q = pt * Qp + lane + 32 * m;
       qj[m] = -1;
-#pragma unroll
-      for (int e = 0; e < EL; ++e) hr[m][e] = 0.f;
       if (q < q_end) {
         const int j = q / C2;
         qj[m] = (j << 16) | (q - j * C2);
         // every CTA reads all of h: copy blockIdx % kHRep, so that the reads
         // of the grid spread over kHRep times as many L2 lines
         const float* src = a.h + (size_t)(blockIdx.x % kHRep) * a.k * a.I + (size_t)q * EL;
+        float hv[EL];
 #pragma unroll
         for (int e = 0; e < EL / 4; ++e) {
           const float4 v = ld_l2_f4(src + 4 * e);
-          hr[m][4 * e] = v.x;
-          hr[m][4 * e + 1] = v.y;
-          hr[m][4 * e + 2] = v.z;
-          hr[m][4 * e + 3] = v.w;
+          hv[4 * e] = v.x;
+          hv[4 * e + 1] = v.y;
+          hv[4 * e + 2] = v.z;
+          hv[4 * e + 3] = v.w;
         }
+        act_set<F>(hr[m], hv);
+      } else {
+        act_zero<F>(hr[m]);
       }
     }
     for (; i < w.n_items; ++i) {

@@ -150,7 +150,7 @@ struct moe_cache {
   int* err_d = nullptr;
   int* verify_d = nullptr;
   GridBar* bar_d = nullptr;       // grid barrier of the fused MLP kernel
-  unsigned* ring_cnt_d = nullptr; // [2 * MOE_MAX_TOPK] landed-chunk counts of the staged kernel's copier
+  unsigned* ring_cnt_d = nullptr; // [3 * MOE_MAX_TOPK] staged kernel: copier's landed-chunk counts, h counts
   RecHdr* hdr_h = nullptr;        // pinned mirror for MEMCPY mode
   int32_t* lists_h = nullptr;
   uint8_t* xs_d[2] = {nullptr, nullptr};
@@ -168,6 +168,7 @@ struct moe_cache {
   bool timing_on = false;
   TimingPool tp[TM_COUNT];
   int32_t* tm_miss_d = nullptr;   // per timed MLP launch: misses of that layer step
+  unsigned long long* tm_span_d = nullptr;   // per timed MLP launch: copier span record [3] (staged kernel)
   size_t tm_miss_cap = 0;
   std::string err;
 };
@@ -234,6 +235,13 @@ void tm_end(moe_cache* c, int cat, int idx, cudaStream_t s) {
 void tm_note_misses(moe_cache* c, int idx, int layer, cudaStream_t s) {
   if (idx < 0 || c->tm_miss_d == nullptr || (size_t)idx >= c->tm_miss_cap) return;
   cudaMemcpyAsync(c->tm_miss_d + idx, &c->hdr_d[layer].n_misses, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+}
+
+// The copier span record of a timed staged-MLP launch (null when timing is
+// off or the record does not fit); the kernel rewrites all of it every launch.
+unsigned long long* tm_span_slot(moe_cache* c, int idx) {
+  if (idx < 0 || c->tm_span_d == nullptr || (size_t)idx >= c->tm_miss_cap) return nullptr;
+  return c->tm_span_d + (size_t)kSpanRecWords * idx;
 }
 
 moe_status wait_event_bounded(moe_cache* c, cudaEvent_t ev, int timeout_ms) {
@@ -385,6 +393,7 @@ moe_status run_copies_and_mlp(moe_cache* c, int layer, cudaStream_t s, const Mlp
     m.copy_cnt = c->ring_cnt_d;
     m.blk_bytes = c->Be;
     const int ti = tm_begin(c, TM_UP, s);
+    m.copy_span = tm_span_slot(c, ti);
     int nl = 1;
     const cudaError_t fe = launch_layer_mlp(c, m, s, &nl);
     if (fe == cudaSuccess) {
@@ -583,7 +592,7 @@ void free_all(moe_cache* c) {
   }
   void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->fstack_d, c->counts_d, c->slot_map_d, c->slot_expert_d,
                  c->slot_stamp_d, c->slot_aux_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
-                 c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->ring_cnt_d, c->tm_miss_d, c->xs_d[0], c->xs_d[1],
+                 c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->ring_cnt_d, c->tm_miss_d, c->tm_span_d, c->xs_d[0], c->xs_d[1],
                  c->logits_stage_d, c->order_d, c->tiles_d, c->ntiles_d, c->gout_d, c->seq_d, c->ready_d};
   for (void* p : dev)
     if (p) cudaFree(p);
@@ -790,8 +799,8 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   CKC(dmalloc((void**)&c->h_d, h_floats * sizeof(float)));
   CKC(dmalloc((void**)&c->err_d, sizeof(int)));
   CKC(dmalloc((void**)&c->bar_d, sizeof(GridBar)));
-  CKC(dmalloc((void**)&c->ring_cnt_d, 2 * MOE_MAX_TOPK * sizeof(unsigned)));
-  CKC(cudaMemset(c->ring_cnt_d, 0, 2 * MOE_MAX_TOPK * sizeof(unsigned)));
+  CKC(dmalloc((void**)&c->ring_cnt_d, 3 * MOE_MAX_TOPK * sizeof(unsigned)));
+  CKC(cudaMemset(c->ring_cnt_d, 0, 3 * MOE_MAX_TOPK * sizeof(unsigned)));
   CKC(dmalloc((void**)&c->seq_d, sizeof(unsigned)));
   CKC(dmalloc((void**)&c->ready_d, (size_t)E * sizeof(unsigned)));
   // zeroed once: the prepare counter never goes back (not even on reset), so
@@ -959,6 +968,7 @@ moe_status moe_forward(moe_cache_t* c, int layer, const void* x_d, const float* 
   // this layer's host rows (in the VMM layout they sit between two layers' pools)
   a.host_lo = (unsigned long long)back_d_of(c, layer);
   a.host_hi = a.host_lo + (unsigned long long)c->E * c->stride;
+  a.h_cnt = c->ring_cnt_d + 2 * MOE_MAX_TOPK;   // zeroed by this step's prepare
   return run_copies_and_mlp(c, layer, s, &a);
 }
 
@@ -1180,10 +1190,15 @@ moe_status moe_cache_set_timing(moe_cache_t* c, int on, int capacity) {
   }
   if (on && c->tm_miss_cap < cap) {
     if (c->tm_miss_d) CK(c, cudaFree(c->tm_miss_d));
+    if (c->tm_span_d) CK(c, cudaFree(c->tm_span_d));
     c->tm_miss_d = nullptr;
+    c->tm_span_d = nullptr;
+    c->tm_miss_cap = 0;
     CK(c, cudaMalloc((void**)&c->tm_miss_d, cap * sizeof(int32_t)));
+    CK(c, cudaMalloc((void**)&c->tm_span_d, (size_t)kSpanRecWords * cap * sizeof(unsigned long long)));
     c->tm_miss_cap = cap;
   }
+  if (on) CK(c, cudaMemset(c->tm_span_d, 0, (size_t)kSpanRecWords * c->tm_miss_cap * sizeof(unsigned long long)));
   c->timing_on = on != 0;
   return MOE_OK;
 }
@@ -1208,6 +1223,35 @@ moe_status moe_cache_read_timing_launches(moe_cache_t* c, float* ms_h, int32_t* 
     }
     if (ms_h) ms_h[i] = v;
     if (misses_h) misses_h[i] = mi[i];
+  }
+  *n = m;
+  return MOE_OK;
+}
+
+moe_status moe_cache_read_copy_spans(moe_cache_t* c, uint64_t* rec_h, int cap, int* n) {
+  if (!c || !n || cap < 0 || (cap > 0 && !rec_h)) return fail(c, MOE_EINVAL, "null argument");
+  CK(c, cudaSetDevice(c->cfg.device));
+  CK(c, cudaDeviceSynchronize());
+  const int avail = (int)c->tp[TM_UP].used;
+  int m = avail < cap ? avail : cap;
+  if (m > (int)c->tm_miss_cap) m = (int)c->tm_miss_cap;
+  if (m <= 0 || c->tm_span_d == nullptr) {
+    *n = 0;
+    return MOE_OK;
+  }
+  std::vector<unsigned long long> raw((size_t)m * kSpanRecWords);
+  CK(c, cudaMemcpy(raw.data(), c->tm_span_d, raw.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+  for (int i = 0; i < m; ++i) {
+    const unsigned long long* r = raw.data() + (size_t)i * kSpanRecWords;
+    const unsigned long long grid = r[1] <= (unsigned long long)kSpanMaxCtas ? r[1] : 0ull;
+    unsigned long long first = ~0ull, last = 0ull;
+    for (unsigned long long b = 0; b < grid; ++b) {
+      if (r[2 + 2 * b] != 0ull && r[2 + 2 * b] < first) first = r[2 + 2 * b];
+      if (r[3 + 2 * b] > last) last = r[3 + 2 * b];
+    }
+    rec_h[3 * (size_t)i] = first;
+    rec_h[3 * (size_t)i + 1] = last;
+    rec_h[3 * (size_t)i + 2] = grid ? r[0] : 0ull;
   }
   *n = m;
   return MOE_OK;

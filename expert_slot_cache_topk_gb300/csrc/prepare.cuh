@@ -295,7 +295,7 @@ __device__ __forceinline__ void prepare_body(const PrepArgs& a, const PrepSmem& 
   }
   if (tid - l0 >= 0 && tid - l0 < ST_COUNT) S.stats[tid - l0] = a.st->stats[tid - l0];
   if (a.ring_cnt != nullptr)
-    for (int q = tid; q < 2 * MOE_MAX_TOPK; q += nthr) a.ring_cnt[q] = 0u;
+    for (int q = tid; q < 3 * MOE_MAX_TOPK; q += nthr) a.ring_cnt[q] = 0u;
   if (tid == 0) *S.bad = 0;
   if (a.do_route) {
     for (int t = tid >> 5; t < a.T; t += nthr / 32)

@@ -414,6 +414,17 @@ moe_status moe_cache_read_timing(moe_cache_t* c, moe_cache_timing* out);
 moe_status moe_cache_read_timing_launches(moe_cache_t* c, float* ms_h, int32_t* misses_h, int cap,
                                           int* n);
 
+/* Copy span of each timed expert-MLP launch (synchronises): for launch i,
+ * rec_h[3i] / rec_h[3i + 1] = %globaltimer ns when the staged kernel's copier
+ * warps issued their first chunk of missed (or bypassed) expert bytes / when
+ * their last chunk had landed in its slot, rec_h[3i + 2] = experts copied in
+ * that launch.  (rec_h[3i + 1] - rec_h[3i]) is the host-link transfer time of
+ * the launch's copies ([Flash-Next 2x32GB] section 3.2, "the cost of one host
+ * read"); records of launches that copied nothing, or that ran another kernel
+ * or copy mode, hold (~0, 0, 0).  Indexed like moe_cache_read_timing_launches.
+ * Up to `cap` records; *n receives the number available. */
+moe_status moe_cache_read_copy_spans(moe_cache_t* c, uint64_t* rec_h, int cap, int* n);
+
 #ifdef __cplusplus
 }
 #endif
