@@ -35,6 +35,8 @@ STATUS_NAME = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ENOMEM", -3: "MOE_ECUDA",
 MOE_SLOT_KIND_SHIFT = 29
 MOE_SLOT_POOL, MOE_SLOT_SCRATCH, MOE_SLOT_COLD = 0 << 29, 1 << 29, 2 << 29
 MOE_FWD_RESIDUAL = 1
+MOE_GEMM_NONE, MOE_GEMM_TC, MOE_GEMM_TMA = 0, 1, 2
+GEMM_KERNEL_NAME = {MOE_GEMM_NONE: "none", MOE_GEMM_TC: "tc", MOE_GEMM_TMA: "tma"}
 
 
 class moe_cache_config(C.Structure):
@@ -67,7 +69,7 @@ class moe_cache_info(C.Structure):
                 ("pool_bytes", C.c_size_t), ("scratch_bytes", C.c_size_t),
                 ("backing_bytes", C.c_size_t), ("copy_mode", C.c_int), ("memcpy_gbs", C.c_double),
                 ("uva_gbs", C.c_double), ("kernel_launches", C.c_uint64),
-                ("scratch_experts", C.c_int), ("table_layout", C.c_int)]
+                ("scratch_experts", C.c_int), ("table_layout", C.c_int), ("gemm_kernel", C.c_int)]
 
 
 class moe_cache_timing(C.Structure):
@@ -247,6 +249,7 @@ class MoECache:
         self._ck(lib().moe_cache_get_info(self._h, C.byref(i)))
         d = {n: getattr(i, n) for n, _ in moe_cache_info._fields_}
         d["copy_mode_name"] = COPY_MODE_NAME[d["copy_mode"]]
+        d["gemm_kernel_name"] = GEMM_KERNEL_NAME.get(d["gemm_kernel"], "?")
         return d
 
     def backing_view(self, layer: int) -> np.ndarray:

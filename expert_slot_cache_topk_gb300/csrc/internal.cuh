@@ -238,5 +238,32 @@ struct GemmBuffers {
 bool moe_gemm_supported(int wdtype, int H, int I, int k);
 cudaError_t moe_gemm_configure(int wdtype);   // call outside capture
 cudaError_t launch_moe_gemm(int wdtype, const MlpArgs& a, const GemmBuffers& b, cudaStream_t s);
+// the grouping (assignments expert by expert, tiles of <= `tile`) and the
+// combine (y[t] = sum over j of the f32 rows, j in order, + x) of both GEMMs
+cudaError_t launch_group(const int32_t* ids, int n, int E, int32_t* order, int4* tiles, int* ntiles, unsigned* work,
+                         int tile, cudaStream_t s);
+cudaError_t launch_combine(int wdtype, const float* out, const void* x, void* y, int T, int k, int H, int residual,
+                           cudaStream_t s);
+
+// ---- launchers (k_moe_gemm_tma.cu): the grouped expert MLP with the weights
+// on the MMA's M side, operands staged by TMA from tensor maps over the pool
+// and the scratch.  cudaErrorNotSupported = use launch_moe_gemm.
+struct MoeTmaMaps;                // host copies of the tensor maps (opaque)
+struct TmaRegions {
+  unsigned long long pool_lo, pool_hi;         // device addresses the pool maps cover
+  unsigned long long pool_pitch, pool_part;    // per layer: pitch, and the device rows at its start
+  unsigned long long scratch_lo, scratch_hi;   // ... and the scratch maps
+  void* xg;                                    // [rows, H] bf16: the activation rows in tile order
+};
+bool moe_gemm_tma_supported(int wdtype, int H, int I, int k);
+// maps over pool [pool, pool + pool_bytes), scratch, xg [n_rows, H] and the
+// bf16 h rows [n_rows, I] at hb; null when the driver gives no encoder
+MoeTmaMaps* moe_gemm_tma_maps(int wdtype, int H, int I, const void* pool, size_t pool_bytes, const void* scratch,
+                              size_t scratch_bytes, const void* xg, const void* hb, size_t n_rows);
+void moe_gemm_tma_maps_free(MoeTmaMaps* m);
+bool moe_gemm_tma_maps_ok(const MoeTmaMaps* m);
+cudaError_t moe_gemm_tma_configure(int wdtype);   // call outside capture
+cudaError_t launch_moe_gemm_tma(int wdtype, const MlpArgs& a, const GemmBuffers& b, const MoeTmaMaps* m,
+                                const TmaRegions& r, cudaStream_t s);
 
 }  // namespace moe

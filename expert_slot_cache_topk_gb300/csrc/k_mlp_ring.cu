@@ -42,6 +42,7 @@
 // for its own copies in flight.
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "internal.cuh"
@@ -118,12 +119,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, unsigned bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+// waits in hardware (the thread is suspended, not spinning) until the phase
+// with this parity completes or about 20 us pass; true if it completed
 __device__ __forceinline__ bool mbar_try(uint32_t bar, unsigned parity) {
   unsigned ok;
-  asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-               : "=r"(ok)
-               : "r"(bar), "r"(parity)
-               : "memory");
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(20000)
+      : "memory");
   return ok != 0;
 }
 // true once the phase with this parity has completed; false after kWaitNs
@@ -288,6 +292,20 @@ struct Q4Act {
   float sc;         // 2^-s (NaN when the chunk holds a NaN or an infinity)
 };
 
+// FP8 activation chunk: 16 values as eight f16 pairs at a power-of-two scale
+// 2^s chosen so that the chunk's largest magnitude times 2^s lies in [8, 16):
+// a product with an E4M3 code (|code| <= 448) stays below 7168 and a half-lane
+// sum of eight below 57344, inside f16.  Codes become f16 pairs exactly
+// (cvt.rn.f16x2.e4m3x2), each 32-bit word of codes meets its activations in
+// two HFMA2, and the chunk's f16 pair of partial sums (eight products each) is
+// summed in f32 and scaled by 2^-s.  x is bf16 (8 significant bits) and fits
+// f16's 11 exactly unless it is below 2^-14 after scaling (2^-18 of the
+// chunk's largest); h (f32) is rounded to 11 bits.
+struct F8Act {
+  uint32_t p[8];   // f16 pairs (x[2i], x[2i + 1]) * 2^s
+  float sc;        // 2^-s (NaN when the chunk holds a NaN or an infinity)
+};
+
 template <int F>
 struct ActSel {
   using type = FAct<FmtT<F>::kElems>;
@@ -295,6 +313,10 @@ struct ActSel {
 template <>
 struct ActSel<MOE_INT4_G128> {
   using type = Q4Act;
+};
+template <>
+struct ActSel<MOE_FP8_E4M3> {
+  using type = F8Act;
 };
 template <int F>
 using ActT = typename ActSel<F>::type;
@@ -344,6 +366,51 @@ __device__ __forceinline__ void q4_pack(const float (&x)[32], Q4Act& a) {
   a.off = -8 * sum;
 }
 
+// 16 activations (f32) -> F8Act
+__device__ __forceinline__ void f8_pack(const float (&x)[16], F8Act& a) {
+  float mx = 0.f;
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float v = fabsf(x[i]);
+    finite = finite && v <= 3.402823466e38f;
+    mx = fmaxf(mx, v);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a.p[i] = 0u;
+  a.sc = 1.f;
+  if (!finite) {
+    a.sc = __int_as_float(0x7fc00000);
+    return;
+  }
+  if (mx < 5.421010862e-20f) return;      // below 2^-64: contributes nothing measurable
+  const int e = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127;
+  const int sh = 3 - e;                                              // mx * 2^sh in [8, 16)
+  const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
+  a.sc = __uint_as_float((uint32_t)(127 - sh) << 23);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __half2 h2 = __floats2half2_rn(x[2 * i] * up, x[2 * i + 1] * up);
+    a.p[i] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+}
+
+// sum over the chunk of code * x * 2^s, as f32 (the caller scales by 2^-s)
+__device__ __forceinline__ float f8_dot(const uint4 w, const F8Act& a) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  __half2 acc = __float2half2_rn(0.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t lo, hi;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((unsigned short)(ws[j] & 0xffffu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((unsigned short)(ws[j] >> 16)));
+    acc = __hfma2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&a.p[2 * j]), acc);
+    acc = __hfma2(*reinterpret_cast<const __half2*>(&hi), *reinterpret_cast<const __half2*>(&a.p[2 * j + 1]), acc);
+  }
+  const float2 f = __half22float2(acc);
+  return f.x + f.y;
+}
+
 __device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
   int d;
   asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -375,6 +442,7 @@ __device__ __forceinline__ int q4_dot(const uint4 w, const Q4Act& a) {
 template <int F>
 __device__ __forceinline__ float chunk_dot_r(const uint4 w, const ActT<F>& x) {
   if constexpr (F == MOE_INT4_G128) return (float)q4_dot(w, x) * x.sc;
+  else if constexpr (F == MOE_FP8_E4M3) return f8_dot(w, x) * x.sc;
   else return chunk_dot<F>(w, x.v);
 }
 
@@ -386,6 +454,10 @@ __device__ __forceinline__ void act_zero(ActT<F>& a) {
     for (int i = 0; i < 16; ++i) a.p[i] = 0u;
     a.off = 0;
     a.sc = 1.f;
+  } else if constexpr (F == MOE_FP8_E4M3) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a.p[i] = 0u;
+    a.sc = 1.f;
   } else {
 #pragma unroll
     for (int e = 0; e < FmtT<F>::kElems; ++e) a.v[e] = 0.f;
@@ -396,6 +468,7 @@ __device__ __forceinline__ void act_zero(ActT<F>& a) {
 template <int F>
 __device__ __forceinline__ void act_set(ActT<F>& a, const float (&v)[FmtT<F>::kElems]) {
   if constexpr (F == MOE_INT4_G128) q4_pack(v, a);
+  else if constexpr (F == MOE_FP8_E4M3) f8_pack(v, a);
   else {
 #pragma unroll
     for (int e = 0; e < FmtT<F>::kElems; ++e) a.v[e] = v[e];

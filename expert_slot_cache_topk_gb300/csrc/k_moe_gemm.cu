@@ -77,10 +77,11 @@ struct GemmArgs {
 // One CTA.  Counts the assignments of every expert, lays them out expert by
 // expert (ascending expert; within an expert in no particular order, which
 // the results do not depend on) and cuts every expert's run into tiles of at
-// most kTileM.
+// most `tile` assignments.
 __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const int32_t* __restrict__ ids, int n, int E,
                                                             int32_t* __restrict__ order, int4* __restrict__ tiles,
-                                                            int* __restrict__ ntiles, unsigned* __restrict__ work) {
+                                                            int* __restrict__ ntiles, unsigned* __restrict__ work,
+                                                            int tile) {
   __shared__ int cnt[MOE_MAX_EXPERTS];
   __shared__ int off[MOE_MAX_EXPERTS];
   __shared__ int toff[MOE_MAX_EXPERTS];
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const int32_t* __res
   __syncthreads();
   // exclusive scans of the counts and of the tile counts (E <= blockDim.x)
   const int c = tid < E ? cnt[tid] : 0;
-  const int t = (c + kTileM - 1) / kTileM;
+  const int t = (c + tile - 1) / tile;
   int ic = c, it = t;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -144,8 +145,8 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const int32_t* __res
   }
   if (tid < E) {
     for (int q = 0; q < t; ++q) {
-      const int rows = c - q * kTileM < kTileM ? c - q * kTileM : kTileM;
-      tiles[toff[tid] + q] = make_int4(off[tid] + q * kTileM, rows, tid, 0);
+      const int rows = c - q * tile < tile ? c - q * tile : tile;
+      tiles[toff[tid] + q] = make_int4(off[tid] + q * tile, rows, tid, 0);
     }
   }
 }
@@ -529,7 +530,7 @@ cudaError_t gemm_impl(const MlpArgs& a, const GemmBuffers& b, cudaStream_t s) {
     per_sm = st.blocks_per_sm;
   }
   const int n = a.T * a.k;
-  k_group<<<1, kGroupThreads, 0, s>>>(b.ids, n, b.E, b.order, b.tiles, b.ntiles, b.work);
+  k_group<<<1, kGroupThreads, 0, s>>>(b.ids, n, b.E, b.order, b.tiles, b.ntiles, b.work, kTileM);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   GemmArgs g{};
@@ -582,6 +583,23 @@ cudaError_t moe_gemm_configure(int wdtype) {
     case MOE_FP8_E4M3: return gemm_configure_impl<MOE_FP8_E4M3>();
   }
   return cudaErrorNotSupported;
+}
+
+cudaError_t launch_group(const int32_t* ids, int n, int E, int32_t* order, int4* tiles, int* ntiles, unsigned* work,
+                         int tile, cudaStream_t s) {
+  k_group<<<1, kGroupThreads, 0, s>>>(ids, n, E, order, tiles, ntiles, work, tile);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int wdtype, const float* out, const void* x, void* y, int T, int k, int H, int residual,
+                           cudaStream_t s) {
+  const long long groups = (long long)T * (H / 4);
+  const unsigned grid = (unsigned)((groups + 255) / 256);
+  if (wdtype == MOE_BF16) k_combine<MOE_BF16><<<grid, 256, 0, s>>>(out, x, y, T, k, H, residual);
+  else if (wdtype == MOE_INT4_G128) k_combine<MOE_INT4_G128><<<grid, 256, 0, s>>>(out, x, y, T, k, H, residual);
+  else if (wdtype == MOE_FP8_E4M3) k_combine<MOE_FP8_E4M3><<<grid, 256, 0, s>>>(out, x, y, T, k, H, residual);
+  else return cudaErrorNotSupported;
+  return cudaGetLastError();
 }
 
 cudaError_t launch_moe_gemm(int wdtype, const MlpArgs& a, const GemmBuffers& b, cudaStream_t s) {

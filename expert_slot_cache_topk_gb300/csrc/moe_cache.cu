@@ -125,6 +125,9 @@ struct moe_cache {
   int4* tiles_d = nullptr;        //               tiles of up to 128 assignments
   int* ntiles_d = nullptr;
   float* gout_d = nullptr;        //               [T*k, H] f32 per-assignment outputs
+  uint8_t* xg_d = nullptr;        //               [T*k, H] bf16 activation rows in tile order (TMA GEMM)
+  MoeTmaMaps* tma = nullptr;      //               tensor maps of the TMA GEMM (null: the cp.async GEMM)
+  size_t scratch_bytes = 0;
   unsigned* seq_d = nullptr;      // prepare counter (RecHdr.seq)
   unsigned* ready_d = nullptr;    // [E] expert e copied in the step with that seq
   std::vector<uint8_t> cold_h;
@@ -363,6 +366,21 @@ cudaError_t launch_layer_mlp(moe_cache* c, const MlpArgs& m, cudaStream_t s, int
       b.ready = c->ready_d;
       b.hdr = c->hdr_d + overlap_layer;
     }
+    if (c->tma != nullptr) {
+      TmaRegions r{};
+      r.pool_lo = (unsigned long long)c->pool_d;
+      r.pool_hi = r.pool_lo + (unsigned long long)c->L * c->pool_pitch;
+      r.pool_pitch = c->pool_pitch;
+      r.pool_part = c->vmm.va ? c->vmm.pool_part : c->pool_pitch;
+      r.scratch_lo = (unsigned long long)c->scratch_d;
+      r.scratch_hi = r.scratch_lo + c->scratch_bytes;
+      r.xg = c->xg_d;
+      const cudaError_t e = launch_moe_gemm_tma(c->wd, m, b, c->tma, r, s);
+      if (e != cudaErrorNotSupported) {
+        *launches = 5;
+        return e;
+      }
+    }
     const cudaError_t e = launch_moe_gemm(c->wd, m, b, s);
     if (e != cudaErrorNotSupported) {
       *launches = 4;
@@ -593,9 +611,10 @@ void free_all(moe_cache* c) {
   void* dev[] = {c->pool_d, c->scratch_d, c->cold_d, c->fstack_d, c->counts_d, c->slot_map_d, c->slot_expert_d,
                  c->slot_stamp_d, c->slot_aux_d, c->state_d, c->hdr_d, c->lists_d, c->asg_d, c->pend_d, c->src_d, c->ids_d,
                  c->w_d, c->h_d, c->err_d, c->verify_d, c->bar_d, c->ring_cnt_d, c->tm_miss_d, c->tm_span_d, c->xs_d[0], c->xs_d[1],
-                 c->logits_stage_d, c->order_d, c->tiles_d, c->ntiles_d, c->gout_d, c->seq_d, c->ready_d};
+                 c->logits_stage_d, c->order_d, c->tiles_d, c->ntiles_d, c->gout_d, c->seq_d, c->ready_d, c->xg_d};
   for (void* p : dev)
     if (p) cudaFree(p);
+  moe_gemm_tma_maps_free(c->tma);
   if (c->backing_h) cudaFreeHost(c->backing_h);
   if (c->hdr_h) cudaFreeHost(c->hdr_h);
   if (c->lists_h) cudaFreeHost(c->lists_h);
@@ -773,6 +792,7 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
     c->pool_pitch = (size_t)c->N * c->stride;
     c->back_pitch = (size_t)c->E * c->stride;
   }
+  c->scratch_bytes = scratch_bytes;
   if ((g.table_layout != MOE_TABLE_VMM && dmalloc((void**)&c->pool_d, pool_bytes) != cudaSuccess) ||
       dmalloc((void**)&c->scratch_d, scratch_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -795,7 +815,10 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   CKC(dmalloc((void**)&c->src_d, TK * sizeof(unsigned long long)));
   CKC(dmalloc((void**)&c->ids_d, TK * sizeof(int32_t)));
   CKC(dmalloc((void**)&c->w_d, TK * sizeof(float)));
-  const size_t h_floats = TK * c->I > mlp_ring_h_floats(c->K, c->I) ? TK * c->I : mlp_ring_h_floats(c->K, c->I);
+  // h: [T*k, I] f32 (per-token kernels), the staged kernel's copies, or (TMA
+  // GEMM) at least 128 rows of bf16 so that every activation box lies inside it
+  size_t h_floats = TK * c->I > mlp_ring_h_floats(c->K, c->I) ? TK * c->I : mlp_ring_h_floats(c->K, c->I);
+  if (h_floats < (size_t)64 * c->I) h_floats = (size_t)64 * c->I;
   CKC(dmalloc((void**)&c->h_d, h_floats * sizeof(float)));
   CKC(dmalloc((void**)&c->err_d, sizeof(int)));
   CKC(dmalloc((void**)&c->bar_d, sizeof(GridBar)));
@@ -830,6 +853,20 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
     CKC(dmalloc((void**)&c->gout_d, TK * c->H * sizeof(float)));
     CKC(moe_gemm_configure(c->wd));
     c->gemm_mlp = true;
+    if (moe_gemm_tma_supported(c->wd, c->H, c->I, c->K)) {
+      // the TMA GEMM: activation rows gathered in tile order, tensor maps over
+      // the pool (device rows of every layer), the scratch and the h rows
+      const size_t rows = TK > 128 ? TK : 128;   // every activation box (<= 128 rows) inside the buffers
+      CKC(dmalloc((void**)&c->xg_d, rows * c->H * 2));
+      CKC(cudaMemset(c->xg_d, 0, rows * c->H * 2));
+      c->tma = moe_gemm_tma_maps(c->wd, c->H, c->I, c->pool_d, (size_t)c->L * c->pool_pitch, c->scratch_d,
+                                 c->scratch_bytes, c->xg_d, c->h_d, rows);
+      if (!moe_gemm_tma_maps_ok(c->tma) || moe_gemm_tma_configure(c->wd) != cudaSuccess) {
+        cudaGetLastError();
+        moe_gemm_tma_maps_free(c->tma);
+        c->tma = nullptr;
+      }
+    }
   }
   int sms = 0;
   CKC(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, g.device));
@@ -864,6 +901,7 @@ moe_status moe_cache_get_info(moe_cache_t* c, moe_cache_info* out) {
   out->kernel_launches = c->launches;
   out->scratch_experts = c->scratch_n;
   out->table_layout = c->cfg.table_layout;
+  out->gemm_kernel = !c->gemm_mlp ? MOE_GEMM_NONE : (c->tma != nullptr ? MOE_GEMM_TMA : MOE_GEMM_TC);
   return MOE_OK;
 }
 

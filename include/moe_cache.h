@@ -244,7 +244,19 @@ typedef struct {
   uint64_t kernel_launches;  /* kernels launched by this handle so far */
   int scratch_experts;       /* bypass scratch capacity in experts */
   int table_layout;          /* moe_table_layout in use */
+  int gemm_kernel;           /* grouped expert MLP of multi-token steps: MOE_GEMM_* */
 } moe_cache_info;
+
+/* moe_cache_info.gemm_kernel: which kernel runs steps of several tokens.
+ *  MOE_GEMM_NONE  the per-token kernels (max_tokens 1, f32 weights, or a shape
+ *                 the tensor-core kernels do not take)
+ *  MOE_GEMM_TC    tcgen05, tokens on M, operands staged with cp.async
+ *  MOE_GEMM_TMA   tcgen05, weight rows on M and tokens on N, operands staged by
+ *                 TMA from tensor maps, warp-specialised (the default when the
+ *                 CUDA driver provides tensor-map encoding) */
+#define MOE_GEMM_NONE 0
+#define MOE_GEMM_TC 1
+#define MOE_GEMM_TMA 2
 
 /* Per-phase GPU time accumulated while timing is on (CUDA events on the
  * stream each kernel is launched on).  Works under stream capture too: the

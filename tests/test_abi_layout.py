@@ -28,6 +28,7 @@ CONSTANTS = {
     "MOE_SLOT_KIND_SHIFT": "MOE_SLOT_KIND_SHIFT", "MOE_SLOT_POOL": "MOE_SLOT_POOL",
     "MOE_SLOT_SCRATCH": "MOE_SLOT_SCRATCH", "MOE_SLOT_COLD": "MOE_SLOT_COLD",
     "MOE_FWD_RESIDUAL": "MOE_FWD_RESIDUAL",
+    "MOE_GEMM_NONE": "MOE_GEMM_NONE", "MOE_GEMM_TC": "MOE_GEMM_TC", "MOE_GEMM_TMA": "MOE_GEMM_TMA",
 }
 
 

@@ -349,22 +349,33 @@ def test_staged_kernel_falls_back_for_shapes_it_cannot_take():
     c.close()
 
 
-@pytest.mark.parametrize("name,T,slots", [("olmoe", 16, None), ("olmoe", 16, 64), ("int4", 24, 64),
-                                          ("int4", 24, 512), ("int4", 3, 16)])
-def test_multi_token_steps_on_the_tensor_cores(name, T, slots):
+# shapes: the workloads' own, and ones whose rows split into items of 128
+# weight rows instead of 256 (hidden 384: 128-row down items; inter 192: 128-row
+# up items), and 8 experts with 96 tokens each (two token tiles per expert)
+@pytest.mark.parametrize("name,T,slots,over", [
+    ("olmoe", 16, None, {}), ("olmoe", 16, 64, {}), ("int4", 24, 64, {}), ("int4", 24, 512, {}), ("int4", 3, 16, {}),
+    ("olmoe", 12, None, {"wdtype": "fp8"}),
+    ("olmoe", 12, None, {"hidden": 384, "inter": 192}),
+    ("olmoe", 12, None, {"hidden": 384, "inter": 192, "wdtype": "fp8"}),
+    ("int4", 12, None, {"hidden": 384, "inter": 384}),
+    ("olmoe", 96, None, {"experts": 8, "slots": 8}),
+    ("int4", 96, None, {"experts": 10, "slots": 10}),
+])
+def test_multi_token_steps_on_the_tensor_cores(name, T, slots, over):
     """Several tokens per step run the grouped tcgen05 GEMM (assignments
     grouped by expert): every token against the float64 oracle, and the
     per-token kernel (mlp_kernel="plain") within the same tolerance."""
-    w = W[name].with_(layers=1, tokens=T)
+    w = W[name].with_(layers=1, tokens=T, **over)
     steps = 3
     lgs = synth.routing_logits(w, 0, steps)
     xs = synth.hidden_states(w, 0, steps)
     wt = OracleWeights(w)
     c = make_cache(w, slots=slots)
+    assert c.info()["gemm_kernel_name"] == "tma"   # weight rows on N, TMA-staged operands
     launches0 = c.info()["kernel_launches"]
     ys = _forward_steps(c, w, 0, xs, lgs)
     per_step = (c.info()["kernel_launches"] - launches0) / steps
-    assert per_step >= 5          # prepare, group, up GEMM, down GEMM, combine (+ copies)
+    assert per_step >= 6          # prepare, group, gather, up GEMM, down GEMM, combine (+ copies)
     c.check()
     c.close()
     cp = make_cache(w, slots=slots, mlp_kernel="plain")
