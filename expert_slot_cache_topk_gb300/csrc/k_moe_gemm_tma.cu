@@ -16,24 +16,26 @@
 // Why weights on N: on this GPU one tcgen05.mma of kind::f16 (M = 64 or 128,
 // K = 16) takes the same time for every N up to 256, so the instruction count
 // sets the cost.  With the weights on N one instruction covers 256 weight
-// rows, with the tokens (a few to 64 per tile) on M = 128; the rows of M past
-// the tile's tokens compute values nobody reads.
+// rows, with the tile's tokens (a few to 64) on M = 64.
 //
-// Warp roles (16 warps, one CTA per SM, items b, b + G, ... of the grid):
-//   warps 0-1  epilogue: tensor-memory lane quadrants 0 and 1 hold the tile's
-//              64 token rows of the accumulator (tcgen05.ld), one token a lane;
-//   warp 2     TMA producer: per stage (one or two K steps of 64) boxes of the
-//              weight rows (bf16, or raw INT4 / FP8 bytes) from tensor maps
-//              over the pool and the bypass scratch, and of the tile's
-//              activation rows; experts in mapped host memory (the cold set,
-//              "Running 125B MoE on Two 32 GB Cards", section 2) are read
-//              with plain 16-byte loads instead; per item a record for the
-//              other roles and (INT4) a bulk copy of the item's scales;
-//   warp 3     MMA issuer: four tcgen05.mma (K = 16) per K step into one of
+// Warp roles (19 warps, one CTA per SM, items b, b + G, ... of the grid):
+//   warps 0-3  epilogue: with M = 64 the accumulator's row 16 q + i sits in
+//              tensor-memory lane 32 q + i, so warp q reads 16 token rows;
+//   warp 4     weight producer: per item a record for the other roles and
+//              (INT4) a bulk copy of the item's scales; bf16 weight tiles, or
+//              stages of raw INT4 / FP8 codes, by cp.async.bulk.tensor from
+//              tensor maps over the pool and the bypass scratch; experts in
+//              mapped host memory (the cold set, "Running 125B MoE on Two
+//              32 GB Cards", section 2) are read with plain 16-byte loads;
+//   warp 5     activation producer: the tile's activation rows, one K step a box;
+//   warp 6     MMA issuer: four tcgen05.mma (K = 16) per K step into one of
 //              two accumulators in tensor memory;
-//   warps 4-15 (INT4 / FP8) three dequantisation groups of four warps; group
+//   warps 7-18 (INT4 / FP8) three dequantisation groups of four warps; group
 //              g turns the raw codes of K steps g, g + 3, ... into a bf16
-//              weight tile in shared memory, two rows a thread.
+//              weight tile in the MMA's layout (a ring of four tiles).
+// Weight tiles, raw stages and activation tiles are three rings, each freed
+// by its own reader, so raw codes stream ahead of the dequantisation and the
+// dequantisation ahead of the MMA.
 // All hand-offs are mbarriers; no CTA-wide barrier runs inside the item loop.
 // Every wait is bounded by the global timer and sets DEVERR_RING when it runs
 // out; the other roles then stop at their next wait.
@@ -66,54 +68,54 @@ namespace {
 using namespace mlp;
 
 constexpr int kDqGroups = 3;           // INT4 / FP8 dequantisation groups of four warps
-constexpr int kWProd = 2, kWMma = 3, kWDq = 4;   // warps 0 and 1: epilogue
+// warps 0-3: epilogue (tensor-memory lane quadrants 0-3)
+constexpr int kWProdW = 4, kWProdA = 5, kWMma = 6, kWDq = 7;
 constexpr int kTWarps = kWDq + 4 * kDqGroups;
 constexpr int kTThreads = 32 * kTWarps;
-constexpr int kTileTok = 64;           // tokens per tile (MMA M = 128)
-constexpr int kM = 128;
-constexpr int kKS = 64;                // K elements per K step (one row of 128 bytes)
-constexpr int kATile = kTileTok * 128; // activation rows of one K step (8 KB)
-constexpr int kAPad = (kM - kTileTok) * 128;   // the MMA reads 128 rows: room past the last activation tile
+constexpr int kTileTok = 64;           // tokens per tile (MMA M = 64)
+constexpr int kM = 64;
+constexpr int kKS = 64;                // K elements per K step
+constexpr int kATile = kTileTok * 128; // activation rows of one K step: 64 rows of 128 bytes (8 KB)
+constexpr int kARing = 4;              // activation tiles in flight
 constexpr int kMaxWN = 256;
-constexpr int kMaxStagesT = 8;
+constexpr int kMaxTiles = 8;           // weight tiles (bf16, in the MMA's layout)
+constexpr int kMaxRaw = 8;             // raw-code stages (INT4 / FP8)
 constexpr int kRecSlots = 8;           // item records in flight
 constexpr int kScSlots = 2;            // INT4: items whose scales are in shared memory
 constexpr unsigned long long kTWaitNs = 500000000ull;   // 0.5 s
 static_assert(kTWarps * 32 <= 1024, "block size");
-static_assert((kWDq & 3) == 0, "a dequantisation group spans the four lane quadrants");
 
-// Per weight format: K steps per stage and raw bytes per weight row and stage
-// (0: bf16, whose rows the MMA reads in place)
+// Per weight format.  Weight tiles hold one K step (rows of 64 bf16, 128
+// bytes, 128-byte swizzle): bf16 tiles land by TMA; INT4 / FP8 raw codes land
+// by TMA in stages of 64-byte rows (two INT4 K steps or one FP8 K step,
+// 64-byte swizzle) and the dequantisation warps write the tiles.
 template <int F>
 struct GT;
 template <>
 struct GT<MOE_BF16> {
-  static constexpr int kSub = 1, kRawRow = 0;
+  static constexpr int kRawSteps = 0;
 };
 template <>
 struct GT<MOE_INT4_G128> {
-  static constexpr int kSub = 2, kRawRow = 64;
+  static constexpr int kRawSteps = 2;
 };
 template <>
 struct GT<MOE_FP8_E4M3> {
-  static constexpr int kSub = 1, kRawRow = 64;
+  static constexpr int kRawSteps = 1;
 };
-// bytes per weight row in a stage
-template <int F>
-__host__ __device__ constexpr int wrow_bytes() { return GT<F>::kRawRow ? GT<F>::kRawRow : 128; }
-template <int F>
-__host__ __device__ constexpr int stage_bytes(int wn) { return wn * wrow_bytes<F>() + GT<F>::kSub * kATile; }
+constexpr int kTRB = 128;              // bytes per weight-tile row
 
 // weight rows per item of a phase: 256 where the rows split evenly, else 128
 __host__ __device__ inline int phase_wn(int ph, int H, int I) {
   return ph == 0 ? (I % 128 == 0 ? 256 : 128) : (H % 256 == 0 ? 256 : 128);
 }
 
-// Dynamic shared memory of a phase: stages, the pad the MMA may read past the
-// last activation tile, the dequantised tiles, the INT4 scale slots.
+// Dynamic shared memory of a phase, in this order: weight tiles, raw stages,
+// activation tiles, INT4 scale slots.
 struct TLayout {
-  int ns = 0;              // stages
-  int wn = 0;              // weight rows per item
+  int wn = 0;              // weight rows per item (MMA N)
+  int nt = 0;              // weight tiles
+  int nr = 0;              // raw stages
   unsigned sc_bytes = 0;   // INT4 scale bytes per slot
   size_t bytes = 0;
 };
@@ -121,17 +123,28 @@ template <int F>
 bool tma_layout(int ph, int H, int I, size_t budget, TLayout* L) {
   const int wn = phase_wn(ph, H, I);
   const int K = ph == 0 ? H : I;
-  const size_t sb = (size_t)stage_bytes<F>(wn);
+  const size_t tb = (size_t)wn * kTRB;
+  const size_t rb = (size_t)wn * 64;
   const size_t sc = F == MOE_INT4_G128 ? (size_t)wn * (K / 128) * 2 : 0;
-  const size_t tiles = F == MOE_BF16 ? 0 : (size_t)kDqGroups * wn * 128;
-  const size_t fixed = (size_t)kAPad + tiles + (size_t)kScSlots * sc + 1024;   // + alignment slack
-  if (budget < fixed + 2 * sb) return false;
-  size_t n = (budget - fixed) / sb;
-  if (n > (size_t)kMaxStagesT) n = kMaxStagesT;
-  L->ns = (int)n;
+  const size_t fixed = (size_t)kARing * kATile + (size_t)kScSlots * sc + 1024;   // + alignment slack
+  if (budget < fixed) return false;
+  size_t nt = 0, nr = 0;
+  if (F == MOE_BF16) {
+    nt = (budget - fixed) / tb;
+    if (nt > (size_t)kMaxTiles) nt = kMaxTiles;
+  } else {
+    nt = 4;   // four K steps of dequantised weights
+    if (budget < fixed + nt * tb) return false;
+    nr = (budget - fixed - nt * tb) / rb;
+    if (nr > (size_t)kMaxRaw) nr = kMaxRaw;
+    if (nr < 2) return false;
+  }
+  if (nt < 3) return false;
   L->wn = wn;
+  L->nt = (int)nt;
+  L->nr = (int)nr;
   L->sc_bytes = (unsigned)sc;
-  L->bytes = n * sb + fixed;
+  L->bytes = nt * tb + nr * rb + fixed;
   return true;
 }
 
@@ -163,24 +176,27 @@ struct TArgs {
   const uint8_t* pending;      // [n] or null: the assignment's expert is copied in this step
   const unsigned* ready;       // [E]: ready[e] == hdr->seq once expert e has landed
   const RecHdr* hdr;
-  int ns;                      // stages
   int wn;                      // weight rows per item (MMA N)
+  int nt;                      // weight tiles
+  int nr;                      // raw stages
   unsigned sc_bytes;           // INT4 scale bytes of one slot (wn rows x K / 128 bf16)
 };
 
-// What the producer tells the epilogue and the dequantisation warps about an item
+// What the weight producer tells the epilogue and the dequantisation warps about an item
 struct ItemRec {
   unsigned long long blk;      // expert block (0: the tile's assignments are invalid)
   int4 td;                     // the tile: first position, rows, expert
 };
 
 struct TShared {
-  unsigned long long full[kMaxStagesT];   // TMA bytes (and the producer's arrive) of a stage
-  unsigned long long empty[kMaxStagesT];  // the MMAs that read a stage are done
-  unsigned long long tfull[kDqGroups];    // group g filled its bf16 weight tile
-  unsigned long long tempty[kDqGroups];   // the MMAs that read it are done
-  unsigned long long rfull[kRecSlots];    // item record written
-  unsigned long long rempty[kRecSlots];   // read by the epilogue and the dequantisation warps
+  unsigned long long tfull[kMaxTiles];    // weight tile written (TMA bytes, or four dequantisation warps)
+  unsigned long long tempty[kMaxTiles];   // the MMAs that read it are done
+  unsigned long long rfull[kMaxRaw];      // raw codes of a stage landed
+  unsigned long long rempty[kMaxRaw];     // every dequantisation unit of the stage has read them
+  unsigned long long afull[kARing];       // activation tile landed
+  unsigned long long aempty[kARing];      // the MMAs that read it are done
+  unsigned long long cfull[kRecSlots];    // item record written
+  unsigned long long cempty[kRecSlots];   // read by the epilogue and the dequantisation warps
   unsigned long long sfull[kScSlots];     // INT4 scales of an item landed
   unsigned long long sempty[kScSlots];    // read by the dequantisation warps
   unsigned long long accf[2];             // accumulator b complete
@@ -210,8 +226,8 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // shared-memory descriptor, K-major, 128-byte swizzle: rows of 128 bytes
-// (64 bf16 of K), 8-row groups 1024 bytes apart; the K = 16 slice j of the
-// rows starts 32 * j bytes in (the swizzle applies to the resulting address)
+// (64 bf16), 8-row groups 1024 bytes apart; the K = 16 slice j of the rows
+// starts 32 * j bytes in (the swizzle applies to the resulting address)
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
   uint64_t d = 0;
   d |= (uint64_t)((addr >> 4) & 0x3FFFu);
@@ -236,20 +252,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2_t(float lo, float hi) {
 // Eight 4-bit codes (nibble i of wd is element i) -> bf16 (q - 8) * scale in
 // element order, two per 32-bit word: a code in the mantissa of a bf16 whose
 // exponent is that of 128 is the value 128 + q exactly; subtracting 136 leaves
-// q - 8 exactly and the product with the scale is the only rounding.
+// q - 8 exactly and the product with the scale is the only rounding.  Per pair
+// of codes: shift, lop3, sub.bf16x2, mul.bf16x2; then byte permutes into
+// element order.
 __device__ __forceinline__ uint4 int4x8_bf16(uint32_t wd, uint32_t scale2) {
-  const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&scale2);
-  const uint32_t off_bits = 0x43084308u;   // bf16x2 {136, 136}
-  const __nv_bfloat162 off = *reinterpret_cast<const __nv_bfloat162*>(&off_bits);
-  uint32_t v[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t p = ((wd >> (4 * j)) & 0x000F000Fu) | 0x43004300u;   // {128 + q_j, 128 + q_j+4}
-    const __nv_bfloat162 d = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162*>(&p), off), s2);
-    v[j] = *reinterpret_cast<const uint32_t*>(&d);
-  }
-  return make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
-                    __byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632));
+  uint32_t v0, v1, v2, v3;
+  asm("{ .reg .b32 t, p, o;\n"
+      "mov.b32 o, 0x43084308;\n"                          // bf16x2 {136, 136}
+      "lop3.b32 p, %4, 0x000F000F, 0x43004300, 0xEA;\n"    // {128 + q0, 128 + q4}
+      "sub.rn.bf16x2 p, p, o;\n"
+      "mul.rn.bf16x2 %0, p, %5;\n"
+      "shr.b32 t, %4, 4;\n"
+      "lop3.b32 p, t, 0x000F000F, 0x43004300, 0xEA;\n"     // {128 + q1, 128 + q5}
+      "sub.rn.bf16x2 p, p, o;\n"
+      "mul.rn.bf16x2 %1, p, %5;\n"
+      "shr.b32 t, %4, 8;\n"
+      "lop3.b32 p, t, 0x000F000F, 0x43004300, 0xEA;\n"     // {128 + q2, 128 + q6}
+      "sub.rn.bf16x2 p, p, o;\n"
+      "mul.rn.bf16x2 %2, p, %5;\n"
+      "shr.b32 t, %4, 12;\n"
+      "lop3.b32 p, t, 0x000F000F, 0x43004300, 0xEA;\n"     // {128 + q3, 128 + q7}
+      "sub.rn.bf16x2 p, p, o;\n"
+      "mul.rn.bf16x2 %3, p, %5; }"
+      : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+      : "r"(wd), "r"(scale2));
+  return make_uint4(__byte_perm(v0, v1, 0x5410), __byte_perm(v2, v3, 0x5410), __byte_perm(v0, v1, 0x7632),
+                    __byte_perm(v2, v3, 0x7632));
 }
 
 // Eight E4M3 codes (byte i of the pair of words is element i) -> bf16, exact
@@ -290,6 +318,20 @@ __device__ __forceinline__ bool warp_wait(TShared& S, uint32_t bar, unsigned par
   return ok;
 }
 
+// The item's expert block and where its weight rows are: region (pool,
+// scratch or none: plain loads) and first row in the region's map
+template <int F, int PH>
+__device__ __forceinline__ void item_weights(const TArgs& g, unsigned long long blk, size_t wrb, int* reg,
+                                             int* row_base) {
+  const unsigned long long wblk = blk + (PH == PH_UP ? 0ull : g.off_w2);
+  *reg = REG_NONE;
+  for (int q = 0; q < 2; ++q)
+    if (blk >= g.reg_lo[q] && blk < g.reg_hi[q] && (blk - g.reg_lo[q]) % g.reg_pitch[q] < g.reg_part[q] &&
+        ((wblk - g.reg_lo[q]) % wrb) == 0ull)
+      *reg = q;
+  *row_base = *reg == REG_NONE ? 0 : (int)((wblk - g.reg_lo[*reg]) / wrb);
+}
+
 template <int F, int PH>
 __global__ void __launch_bounds__(kTThreads, 1)
     k_moe_gemm_tma(const __grid_constant__ TmaMaps maps, TArgs g) {
@@ -297,16 +339,17 @@ __global__ void __launch_bounds__(kTThreads, 1)
   __shared__ TShared S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr bool kDq = F != MOE_BF16;
-  constexpr int kSub = GT<F>::kSub;               // K steps per stage
-  constexpr int RB = wrow_bytes<F>();             // bytes per weight row in a stage
-  constexpr unsigned kRecReaders = 2 + (kDq ? 4 * kDqGroups : 0);
-  const int NS = g.ns;
-  const int WN = g.wn;
-  const int SB = stage_bytes<F>(WN);
-  const int WB = WN * RB;                         // weight part of a stage
+  constexpr int kRawSteps = GT<F>::kRawSteps;     // K steps per raw stage
+  constexpr int kUnitsPerRaw = kRawSteps > 0 ? kRawSteps : 1;   // dequantisation units reading one raw stage
+  constexpr unsigned kRecReaders = 4 + (kDq ? 4 * kDqGroups : 0);
+  const int WN = g.wn, NTL = g.nt, NR = g.nr;
+  const int TB = WN * kTRB;                       // bytes per weight tile
+  const int RSB = WN * 64;                        // bytes per raw stage
   uint8_t* base = smem + ((1024u - (tc::smem_u32(smem) & 1023u)) & 1023u);
-  uint8_t* tiles = base + (size_t)NS * SB + kAPad;                                  // [kDqGroups][WN rows x 128 B]
-  uint8_t* scb = tiles + (kDq ? (size_t)kDqGroups * WN * 128 : 0);                  // [kScSlots][sc_bytes]
+  uint8_t* tiles = base;                                          // [nt][WN rows x 128]
+  uint8_t* raws = tiles + (size_t)NTL * TB;                       // [nr][WN rows x 64]
+  uint8_t* acts = raws + (size_t)NR * RSB;                        // [kARing][64 rows x 128]
+  uint8_t* scb = acts + (size_t)kARing * kATile;                  // [kScSlots][sc_bytes]
   const int K = PH == PH_UP ? g.H : g.I;
   const int nk = K / kKS;
   const int NT = PH == PH_UP ? g.I / (WN >> 1) : g.H / WN;
@@ -314,17 +357,21 @@ __global__ void __launch_bounds__(kTThreads, 1)
   const int items = ntiles * NT;
   const size_t wrb = F == MOE_BF16 ? (size_t)K * 2 : (F == MOE_FP8_E4M3 ? (size_t)K : (size_t)K / 2);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      tc::mbar_init(tc::smem_u32(&S.full[s]), 1u);
-      tc::mbar_init(tc::smem_u32(&S.empty[s]), 1u);
-    }
-    for (int b = 0; b < kDqGroups; ++b) {
-      tc::mbar_init(tc::smem_u32(&S.tfull[b]), 4u);
+    for (int b = 0; b < NTL; ++b) {
+      tc::mbar_init(tc::smem_u32(&S.tfull[b]), kDq ? 4u : 1u);
       tc::mbar_init(tc::smem_u32(&S.tempty[b]), 1u);
     }
-    for (int b = 0; b < kRecSlots; ++b) {
+    for (int b = 0; b < NR; ++b) {
       tc::mbar_init(tc::smem_u32(&S.rfull[b]), 1u);
-      tc::mbar_init(tc::smem_u32(&S.rempty[b]), kRecReaders);
+      tc::mbar_init(tc::smem_u32(&S.rempty[b]), 4u * kUnitsPerRaw);
+    }
+    for (int b = 0; b < kARing; ++b) {
+      tc::mbar_init(tc::smem_u32(&S.afull[b]), 1u);
+      tc::mbar_init(tc::smem_u32(&S.aempty[b]), 1u);
+    }
+    for (int b = 0; b < kRecSlots; ++b) {
+      tc::mbar_init(tc::smem_u32(&S.cfull[b]), 1u);
+      tc::mbar_init(tc::smem_u32(&S.cempty[b]), kRecReaders);
     }
     for (int b = 0; b < kScSlots; ++b) {
       tc::mbar_init(tc::smem_u32(&S.sfull[b]), 1u);
@@ -332,7 +379,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tc::smem_u32(&S.accf[b]), 1u);
-      tc::mbar_init(tc::smem_u32(&S.acce[b]), 2u);
+      tc::mbar_init(tc::smem_u32(&S.acce[b]), 4u);
     }
     S.stop = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -343,9 +390,9 @@ __global__ void __launch_bounds__(kTThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = S.tmem;
 
-  if (warp == kWProd) {
-    // ------------------------------------------------------------ producer
-    unsigned gst = 0;   // stages issued
+  if (warp == kWProdW) {
+    // ------------------------------------------------------- weight producer
+    unsigned gq = 0;    // weight tiles (bf16) or raw stages (INT4 / FP8) issued
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++it) {
@@ -353,16 +400,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
       const int4 td = g.tiles[tile];
       const int asg0 = g.order[td.x];
       const unsigned long long blk = g.asg_ptr[asg0];
-      const unsigned long long wblk = blk + (PH == PH_UP ? 0ull : g.off_w2);
-      int reg = REG_NONE;
-      for (int q = 0; q < 2; ++q)
-        if (blk >= g.reg_lo[q] && blk < g.reg_hi[q] && (blk - g.reg_lo[q]) % g.reg_pitch[q] < g.reg_part[q] &&
-            ((wblk - g.reg_lo[q]) % wrb) == 0ull)
-          reg = q;
-      const int row_base = reg == REG_NONE ? 0 : (int)((wblk - g.reg_lo[reg]) / wrb);
-      // tile rows -> the smallest activation box that holds them
-      const int bi = td.y <= 16 ? 0 : (td.y <= 32 ? 1 : 2);
-      const int brows = 16 << bi;
+      int reg, row_base;
+      item_weights<F, PH>(g, blk, wrb, &reg, &row_base);
       if (PH == PH_UP && g.pending != nullptr && g.pending[asg0] != 0 && lane == 0) {
         // the expert is being copied in this step: wait (bounded) until its copy is published
         const unsigned want = g.hdr->seq;
@@ -384,17 +423,18 @@ __global__ void __launch_bounds__(kTThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       // the item's record for the epilogue and the dequantisation warps
-      const int rsl = it % kRecSlots;
+      const int csl = it % kRecSlots;
       if (it >= kRecSlots &&
-          !warp_wait(S, tc::smem_u32(&S.rempty[rsl]), ((it / kRecSlots) - 1) & 1, g.err, lane, kSleepLong)) {
+          !warp_wait(S, tc::smem_u32(&S.cempty[csl]), ((it / kRecSlots) - 1) & 1, g.err, lane, kSleepLong)) {
         ok = false;
         break;
       }
       if (lane == 0) {
-        S.rec[rsl].blk = blk;
-        S.rec[rsl].td = td;
-        mbar_arrive(tc::smem_u32(&S.rfull[rsl]));
+        S.rec[csl].blk = blk;
+        S.rec[csl].td = td;
+        mbar_arrive(tc::smem_u32(&S.cfull[csl]));
       }
+      const int half = WN >> 1;
       if (F == MOE_INT4_G128) {
         // the scales of the item's WN rows, K / 128 bf16 per row: up = WN/2
         // gate rows from mt * WN/2 and WN/2 up rows from I + mt * WN/2;
@@ -408,7 +448,6 @@ __global__ void __launch_bounds__(kTThreads, 1)
         const uint32_t sfull = tc::smem_u32(&S.sfull[ssl]);
         if (blk != 0ull) {
           const int gpr = K / 128;
-          const int half = WN >> 1;
           const uint8_t* s0 = reinterpret_cast<const uint8_t*>(blk + (PH == PH_UP ? g.off_s13 : g.off_s2));
           const uint8_t* src0 = s0 + (size_t)(PH == PH_UP ? mt * half : mt * WN) * gpr * 2;
           const uint8_t* src1 = s0 + (size_t)(g.I + mt * half) * gpr * 2;
@@ -436,55 +475,83 @@ __global__ void __launch_bounds__(kTThreads, 1)
           if (lane == 0) mbar_arrive(sfull);
         }
       }
-      for (int kt = 0; kt < nk / kSub; ++kt, ++gst) {
-        const int s = (int)(gst % (unsigned)NS);
-        if (gst >= (unsigned)NS &&
-            !warp_wait(S, tc::smem_u32(&S.empty[s]), ((gst / NS) - 1u) & 1u, g.err, lane, kSleepShort)) {
+      // bf16: one weight tile per K step; INT4 / FP8: one raw stage per kRawSteps K steps
+      const int nq = kDq ? nk / kRawSteps : nk;
+      const int nslots = kDq ? NR : NTL;
+      for (int kq = 0; kq < nq; ++kq, ++gq) {
+        const int sl = (int)(gq % (unsigned)nslots);
+        unsigned long long* fb = kDq ? &S.rfull[sl] : &S.tfull[sl];
+        unsigned long long* eb = kDq ? &S.rempty[sl] : &S.tempty[sl];
+        if (gq >= (unsigned)nslots &&
+            !warp_wait(S, tc::smem_u32(eb), ((gq / nslots) - 1u) & 1u, g.err, lane, kSleepShort)) {
           ok = false;
           break;
         }
-        uint8_t* st = base + (size_t)s * SB;
-        const uint32_t w_u = tc::smem_u32(st), a_u = w_u + (uint32_t)WB;
-        const uint32_t full = tc::smem_u32(&S.full[s]);
-        const int k0 = kt * kSub * kKS;                 // first K element of the stage
-        const unsigned abytes = (unsigned)(kSub * brows * 128);
-        const unsigned wbytes = reg == REG_NONE ? 0u : (unsigned)WB;
-        if (reg == REG_NONE && blk != 0ull) {
-          // weights in host memory (or not addressable through a map): plain
-          // loads, stored in the layout the TMA would write
-          const uint8_t* wb = reinterpret_cast<const uint8_t*>(wblk);
-          constexpr int cpr = RB / 16;
-          for (int v = lane; v < WN * cpr; v += 32) {
-            const int r = v / cpr, c = v - r * cpr;
-            const uint4 q = __ldcg(reinterpret_cast<const uint4*>(
-                wb + (size_t)wrow_of<PH>(r, mt, g.I, WN) * wrb + (kDq ? (size_t)kt * RB : (size_t)k0 * 2) + c * 16));
-            *reinterpret_cast<uint4*>(st + (size_t)r * RB + swz_chunk(c, r, RB) * 16) = q;
+        uint8_t* dst = kDq ? raws + (size_t)sl * RSB : tiles + (size_t)sl * TB;
+        constexpr int RB = kDq ? 64 : 128;             // bytes per row of what lands here
+        const int x = kDq ? kq * 64 : kq * kKS;        // bytes of raw codes, or bf16 elements
+        if (reg == REG_NONE) {
+          if (blk != 0ull) {
+            // weights in host memory (or not addressable through a map): plain
+            // loads, stored in the layout the TMA would write
+            const uint8_t* wb = reinterpret_cast<const uint8_t*>(blk + (PH == PH_UP ? 0ull : g.off_w2));
+            constexpr int cpr = RB / 16;
+            for (int v = lane; v < WN * cpr; v += 32) {
+              const int r = v / cpr, c = v - r * cpr;
+              const uint4 q = __ldcg(reinterpret_cast<const uint4*>(
+                  wb + (size_t)wrow_of<PH>(r, mt, g.I, WN) * wrb + (size_t)x * (kDq ? 1 : 2) + c * 16));
+              *reinterpret_cast<uint4*>(dst + (size_t)r * RB + swz_chunk(c, r, RB) * 16) = q;
+            }
+            if (!kDq) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> MMA reads
           }
-          if (!kDq) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> MMA reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tc::smem_u32(fb));
+        } else {
+          if (lane == 0) {
+            mbar_arrive_tx(tc::smem_u32(fb), (unsigned)(WN * RB));
+            const CUtensorMap* wm = &maps.w[reg];
+            const uint32_t d = tc::smem_u32(dst);
+            if (PH == PH_UP) {
+              // WN/2 gate rows, then WN/2 up rows of features mt * WN/2 ..
+              tma_load_2d(d, wm, x, row_base + mt * half, tc::smem_u32(fb));
+              tma_load_2d(d + (uint32_t)(half * RB), wm, x, row_base + g.I + mt * half, tc::smem_u32(fb));
+            } else {
+              tma_load_2d(d, wm, x, row_base + mt * WN, tc::smem_u32(fb));
+            }
+          }
           __syncwarp();
         }
-        if (lane == 0) mbar_arrive_tx(full, abytes + wbytes);
-        __syncwarp();
-        // activation rows of the tile: one box of brows x 64 elements per K step
-        if (lane < kSub) tma_load_2d(a_u + (uint32_t)lane * kATile, &maps.b[bi], k0 + kKS * lane, td.x, full);
-        if (reg != REG_NONE) {
-          const CUtensorMap* wm = &maps.w[reg];
-          const int x = kDq ? kt * RB : k0;             // bytes of raw codes, or bf16 elements
-          const int half = WN >> 1;
-          if (PH == PH_UP) {
-            // WN/2 gate rows, then WN/2 up rows of features mt * WN/2 ..
-            if (lane == 8) tma_load_2d(w_u, wm, x, row_base + mt * half, full);
-            if (lane == 9) tma_load_2d(w_u + (uint32_t)(half * RB), wm, x, row_base + g.I + mt * half, full);
-          } else {
-            if (lane == 8) tma_load_2d(w_u, wm, x, row_base + mt * WN, full);
-          }
-        }
       }
+    }
+  } else if (warp == kWProdA) {
+    // --------------------------------------------------- activation producer
+    unsigned ga = 0;    // activation tiles issued
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+      const int4 td = g.tiles[item / NT];
+      // tile rows -> the smallest box that holds them
+      const int bi = td.y <= 16 ? 0 : (td.y <= 32 ? 1 : 2);
+      const unsigned abytes = (unsigned)((16 << bi) * 128);
+      bool ok = true;
+      for (int ks = 0; ks < nk; ++ks, ++ga) {
+        const int sl = (int)(ga % kARing);
+        if (ga >= (unsigned)kARing &&
+            !warp_wait(S, tc::smem_u32(&S.aempty[sl]), ((ga / kARing) - 1u) & 1u, g.err, lane, kSleepShort)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = tc::smem_u32(&S.afull[sl]);
+          mbar_arrive_tx(fb, abytes);
+          tma_load_2d(tc::smem_u32(acts + (size_t)sl * kATile), &maps.b[bi], ks * kKS, td.x, fb);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
     }
   } else if (warp == kWMma) {
     // ----------------------------------------------------------------- MMA
     const uint32_t idesc = tc::idesc_bf16(kM, (uint32_t)WN);
-    unsigned gs = 0;   // K steps issued
+    unsigned ga = 0, gt = 0;   // activation tiles and weight tiles consumed
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++it) {
@@ -495,29 +562,28 @@ __global__ void __launch_bounds__(kTThreads, 1)
       }
       tc::fence_after_sync();
       const uint32_t d_tmem = tmem + (uint32_t)(buf * kMaxWN);
-      for (int ks = 0; ks < nk; ++ks, ++gs) {
-        const unsigned gt = gs / kSub;                 // its stage
-        const int u = (int)(gs % kSub);
-        const int s = (int)(gt % (unsigned)NS);
-        const int tb = (int)(gs % kDqGroups);
-        if (lane == 0) {
-          ok = wait_or_stop(S, tc::smem_u32(&S.full[s]), (gt / NS) & 1u, g.err);
-          if (ok && kDq) ok = wait_or_stop(S, tc::smem_u32(&S.tfull[tb]), (gs / kDqGroups) & 1u, g.err);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        tc::fence_after_sync();
-        if (lane == 0) {
-          const uint32_t st_u = tc::smem_u32(base + (size_t)s * SB);
-          const uint32_t a_u = st_u + (uint32_t)WB + (uint32_t)(u * kATile);
-          const uint32_t b_u = kDq ? tc::smem_u32(tiles + (size_t)tb * WN * 128) : st_u;
+      for (int ks = 0; ks < nk && ok; ++ks, ++ga) {
+        const int as = (int)(ga % kARing);
+        if (lane == 0) ok = wait_or_stop(S, tc::smem_u32(&S.afull[as]), (ga / kARing) & 1u, g.err);
+        const uint32_t a_u = tc::smem_u32(acts + (size_t)as * kATile);
+        {
+          const int tb = (int)(gt % (unsigned)NTL);
+          if (lane == 0 && ok) ok = wait_or_stop(S, tc::smem_u32(&S.tfull[tb]), (gt / NTL) & 1u, g.err);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc::fence_after_sync();
+          if (lane == 0) {
+            const uint32_t b_u = tc::smem_u32(tiles + (size_t)tb * TB);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tc::mma_bf16(d_tmem, desc_sw128(a_u + (uint32_t)j * 32u), desc_sw128(b_u + (uint32_t)j * 32u), idesc,
-                         (ks | j) != 0 ? 1u : 0u);
-          if (u == kSub - 1) tc::mma_commit(tc::smem_u32(&S.empty[s]));   // the stage's last K step
-          if (kDq) tc::mma_commit(tc::smem_u32(&S.tempty[tb]));
+            for (int j = 0; j < 4; ++j)
+              tc::mma_bf16(d_tmem, desc_sw128(a_u + (uint32_t)j * 32u), desc_sw128(b_u + (uint32_t)j * 32u), idesc,
+                           (ks | j) != 0 ? 1u : 0u);
+            tc::mma_commit(tc::smem_u32(&S.tempty[tb]));
+          }
+          __syncwarp();
+          ++gt;
         }
+        if (lane == 0) tc::mma_commit(tc::smem_u32(&S.aempty[as]));
         __syncwarp();
       }
       if (!ok) break;
@@ -525,65 +591,67 @@ __global__ void __launch_bounds__(kTThreads, 1)
       __syncwarp();
     }
     // every MMA issued has completed before tensor memory is freed
-    if (gs > 0 && lane == 0) {
-      const unsigned last = (gs - 1u) / kSub;          // the last stage
-      tc::mbar_wait(tc::smem_u32(&S.empty[last % (unsigned)NS]), (last / NS) & 1u, kTWaitNs);
+    if (ga > 0 && lane == 0) {
+      const unsigned last = ga - 1u;
+      tc::mbar_wait(tc::smem_u32(&S.aempty[last % kARing]), (last / kARing) & 1u, kTWaitNs);
     }
     __syncwarp();
   } else if (warp >= kWDq) {
     // ------------------------------------------------- dequantisation warps
-    // group grp takes the K steps q with q % kDqGroups == grp and writes them
-    // into its bf16 tile; warp w of the group converts rows w * WN / 4 ..,
-    // WN / 128 a thread
+    // A unit is one weight tile: WN rows x one K step.  Group grp takes the
+    // units u with u % kDqGroups == grp; warp w of the group converts rows
+    // w * WN / 4 .., WN / 128 a thread.
     if (kDq) {
       const int grp = (warp - kWDq) >> 2;
       const int wq = (warp - kWDq) & 3;
       const int gpr = K / 128;                              // INT4 scale groups per row
-      uint8_t* tile_g = tiles + (size_t)grp * WN * 128;
-      unsigned gs = 0;
+      const int upi = nk;                                   // units per item
+      unsigned gu = 0;                                      // units of earlier items
       int it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++it) {
-        const int rsl = it % kRecSlots, ssl = it % kScSlots;
-        if (!warp_wait(S, tc::smem_u32(&S.rfull[rsl]), (it / kRecSlots) & 1, g.err, lane, kSleepShort)) {
+        const int csl = it % kRecSlots, ssl = it % kScSlots;
+        if (!warp_wait(S, tc::smem_u32(&S.cfull[csl]), (it / kRecSlots) & 1, g.err, lane, kSleepShort)) {
           ok = false;
           break;
         }
-        const unsigned long long blk = S.rec[rsl].blk;
+        const unsigned long long blk = S.rec[csl].blk;
         __syncwarp();
-        if (lane == 0) mbar_arrive(tc::smem_u32(&S.rempty[rsl]));
+        if (lane == 0) mbar_arrive(tc::smem_u32(&S.cempty[csl]));
         if (F == MOE_INT4_G128 &&
             !warp_wait(S, tc::smem_u32(&S.sfull[ssl]), (it / kScSlots) & 1, g.err, lane, kSleepShort)) {
           ok = false;
           break;
         }
         const uint16_t* sct = reinterpret_cast<const uint16_t*>(scb + (size_t)ssl * g.sc_bytes);
-        for (int ks = (int)((unsigned)(grp + kDqGroups) - gs % kDqGroups) % kDqGroups; ks < nk; ks += kDqGroups) {
-          const unsigned q = gs + (unsigned)ks;        // K step; stage q / kSub, part q % kSub
-          const unsigned qt = q / kSub;
-          const int u = (int)(q % kSub);
-          const int s = (int)(qt % (unsigned)NS);
+        for (int v = (int)((unsigned)(grp + kDqGroups) - gu % kDqGroups) % kDqGroups; v < upi; v += kDqGroups) {
+          const unsigned u = gu + (unsigned)v;               // unit; its weight tile u % nt
+          const unsigned rq = u / kUnitsPerRaw;               // its raw stage
+          const int part = (int)(u % kUnitsPerRaw);           // which K step of the raw row
+          const int rs = (int)(rq % (unsigned)NR), tb = (int)(u % (unsigned)NTL);
           if (lane == 0) {
-            ok = wait_or_stop(S, tc::smem_u32(&S.full[s]), (qt / NS) & 1u, g.err, kSleepShort);
+            ok = wait_or_stop(S, tc::smem_u32(&S.rfull[rs]), (rq / NR) & 1u, g.err, kSleepShort);
             // the tile free: the MMAs that read its previous contents are done
-            if (ok && q >= (unsigned)kDqGroups)
-              ok = wait_or_stop(S, tc::smem_u32(&S.tempty[grp]), ((q / kDqGroups) - 1u) & 1u, g.err, kSleepShort);
+            if (ok && u >= (unsigned)NTL)
+              ok = wait_or_stop(S, tc::smem_u32(&S.tempty[tb]), ((u / NTL) - 1u) & 1u, g.err, kSleepShort);
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           __syncwarp();
           if (blk != 0ull) {
-            const uint8_t* st = base + (size_t)s * SB;
+            const uint8_t* rst = raws + (size_t)rs * RSB;
+            uint8_t* tile = tiles + (size_t)tb * TB;
 #pragma unroll 1
             for (int h = 0; h < WN / 128; ++h) {
               const int r = wq * (WN / 4) + h * 32 + lane;   // weight row of the item (< WN)
-              const uint8_t* raw = st + (size_t)r * RB;
+              const uint8_t* raw = rst + (size_t)r * 64;
               uint4 o[8];
               if (F == MOE_INT4_G128) {
-                const uint32_t sb = sct[(size_t)r * gpr + (ks >> 1)];
+                // 64 codes = chunks 2 part, 2 part + 1 of the row; K step v is in scale group v / 2
+                const uint32_t sb = sct[(size_t)r * gpr + (v >> 1)];
                 const uint32_t s2 = sb | (sb << 16);
-                const uint4 q0 = reinterpret_cast<const uint4*>(raw)[swz_chunk(2 * u, r, RB)];
-                const uint4 q1 = reinterpret_cast<const uint4*>(raw)[swz_chunk(2 * u + 1, r, RB)];
+                const uint4 q0 = reinterpret_cast<const uint4*>(raw)[swz_chunk(2 * part, r, 64)];
+                const uint4 q1 = reinterpret_cast<const uint4*>(raw)[swz_chunk(2 * part + 1, r, 64)];
                 o[0] = int4x8_bf16(q0.x, s2);
                 o[1] = int4x8_bf16(q0.y, s2);
                 o[2] = int4x8_bf16(q0.z, s2);
@@ -593,50 +661,55 @@ __global__ void __launch_bounds__(kTThreads, 1)
                 o[6] = int4x8_bf16(q1.z, s2);
                 o[7] = int4x8_bf16(q1.w, s2);
               } else {
+                // 64 codes = the whole row
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                  const uint4 v = reinterpret_cast<const uint4*>(raw)[swz_chunk(c, r, RB)];
-                  o[2 * c] = fp8x8_bf16(v.x, v.y);
-                  o[2 * c + 1] = fp8x8_bf16(v.z, v.w);
+                  const uint4 q = reinterpret_cast<const uint4*>(raw)[swz_chunk(c, r, 64)];
+                  o[2 * c] = fp8x8_bf16(q.x, q.y);
+                  o[2 * c + 1] = fp8x8_bf16(q.z, q.w);
                 }
               }
-              uint8_t* trow = tile_g + (size_t)r * 128;
+              uint8_t* trow = tile + (size_t)r * kTRB;
 #pragma unroll
-              for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(trow + swz_chunk(c, r, 128) * 16) = o[c];
+              for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(trow + swz_chunk(c, r, kTRB) * 16) = o[c];
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> MMA reads
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(tc::smem_u32(&S.tfull[grp]));
+          if (lane == 0) {
+            mbar_arrive(tc::smem_u32(&S.tfull[tb]));
+            mbar_arrive(tc::smem_u32(&S.rempty[rs]));
+          }
         }
         if (!ok) break;
-        gs += (unsigned)nk;
+        gu += (unsigned)upi;
         if (F == MOE_INT4_G128) {
           __syncwarp();
           if (lane == 0) mbar_arrive(tc::smem_u32(&S.sempty[ssl]));
         }
       }
     }
-  } else if (warp < 2) {
+  } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
-    // warp q reads lane quadrant q of the accumulator: token rows 32 q .. 32 q + 31
+    // with M = 64 the accumulator's row 16 q + i is in lane 32 q + i: warp q
+    // reads lane quadrant q, its lanes 0-15 hold token rows 16 q .. 16 q + 15
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int half = WN >> 1;
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++it) {
       const int mt = item % NT;
-      const int rsl = it % kRecSlots;
-      if (!warp_wait(S, tc::smem_u32(&S.rfull[rsl]), (it / kRecSlots) & 1, g.err, lane, kSleepLong)) {
+      const int csl = it % kRecSlots;
+      if (!warp_wait(S, tc::smem_u32(&S.cfull[csl]), (it / kRecSlots) & 1, g.err, lane, kSleepLong)) {
         ok = false;
         break;
       }
-      const int4 td = S.rec[rsl].td;
-      const unsigned long long blk = S.rec[rsl].blk;
+      const int4 td = S.rec[csl].td;
+      const unsigned long long blk = S.rec[csl].blk;
       __syncwarp();
-      if (lane == 0) mbar_arrive(tc::smem_u32(&S.rempty[rsl]));
-      const int t = warp * 32 + lane;                  // token row of the tile
-      const bool valid = t < td.y;
+      if (lane == 0) mbar_arrive(tc::smem_u32(&S.cempty[csl]));
+      const int t = warp * 16 + lane;                  // token row of the tile (lanes 0-15)
+      const bool valid = lane < 16 && t < td.y;
       const int pos = td.x + t;
       const int a = valid ? g.order[pos] : 0;          // the row's assignment
       const int buf = it & 1;
@@ -941,15 +1014,17 @@ cudaError_t tma_impl(const MlpArgs& a, const GemmBuffers& b, const MoeTmaMaps& m
   g.pending = b.pending;
   g.ready = b.ready;
   g.hdr = b.hdr;
-  g.ns = lu.ns;
   g.wn = lu.wn;
+  g.nt = lu.nt;
+  g.nr = lu.nr;
   g.sc_bytes = lu.sc_bytes;
   k_moe_gemm_tma<F, PH_UP><<<sms, kTThreads, lu.bytes, s>>>(m.up, g);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   g.pending = nullptr;   // every expert has landed before the up kernel ended
-  g.ns = ld.ns;
   g.wn = ld.wn;
+  g.nt = ld.nt;
+  g.nr = ld.nr;
   g.sc_bytes = ld.sc_bytes;
   k_moe_gemm_tma<F, PH_DOWN><<<sms, kTThreads, ld.bytes, s>>>(m.down, g);
   e = cudaGetLastError();
