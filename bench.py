@@ -176,7 +176,7 @@ def peaks() -> dict:
 # misses, from ncu captures of the source whose tag is the key (null once the
 # kernel source differs from the profiled one).
 MEASURED_TRAFFIC = {
-    ("olmoe", "k_mlp_ring.cu:d08a8647eee599d1"): 103_437_312,
+    ("olmoe", "k_mlp_ring.cu:9d074a0c06c89772"): 103_348_224,
 }
 
 
@@ -656,7 +656,7 @@ def batched_decode(args, dev, world, src, pk) -> dict:
         out["points"].append({
             "slots": N, "value": toks / max_sec, "unit": UNIT, "ms_per_step": 1e3 * max_sec / run.steps,
             "bypass_fraction": cc["bypass_steps"] / (run.steps * w.layers), "hit_rate": cc["hit_rate"],
-            "grouped_gemm": {"kernel": "k_moe_gemm (tcgen05: group + up + down + combine)", "bound": "tensor",
+            "grouped_gemm": {"kernel": "k_moe_gemm_tma (tcgen05, weight rows on N: group + gather + up + down + combine)", "bound": "tensor",
                              "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                              "frac": (tflops / pk["bf16_tflops"]) if tflops else None,
                              "ms_per_layer": 1e3 * gemm_s / (run.steps * w.layers),
@@ -740,7 +740,7 @@ def run_prefill(args, dev, world, src, pk):
                      f"{' (bypass)' if w.slots < w.experts - w.n_cold else ' (all non-cold resident)'}, "
                      f"{w.n_cold} cold experts/layer read in place"),
         "value": all_tok / max_sec, "unit": "tok/s", "ms_per_chunk": 1e3 * max_sec / reps, "chunks": reps,
-        "grouped_gemm": {"kernel": "k_moe_gemm (tcgen05, group + up + down + combine)",
+        "grouped_gemm": {"kernel": "k_moe_gemm_tma (tcgen05, weight rows on N: group + gather + up + down + combine)",
                          "bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": (tflops / pk["bf16_tflops"]) if tflops else None,
                          "flops_per_chunk": flops // reps, "ms_per_chunk": 1e3 * gemm_s / reps,

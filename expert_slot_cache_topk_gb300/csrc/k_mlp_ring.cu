@@ -119,14 +119,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, unsigned bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-// waits in hardware (the thread is suspended, not spinning) until the phase
-// with this parity completes or about 20 us pass; true if it completed
+// true if the phase with this parity has completed; if not, the thread is
+// suspended in hardware (not spinning) until it completes or a system time
+// limit (a few microseconds) passes
 __device__ __forceinline__ bool mbar_try(uint32_t bar, unsigned parity) {
   unsigned ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(20000)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }

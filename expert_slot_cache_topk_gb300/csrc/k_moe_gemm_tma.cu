@@ -302,6 +302,7 @@ constexpr unsigned kSleepNone = 0, kSleepShort = 64, kSleepLong = 256;
 // bounded wait; on a time-out flags the error and asks every role to stop
 __device__ __forceinline__ bool wait_or_stop(TShared& S, uint32_t bar, unsigned parity, int* err,
                                              unsigned sleep_ns = kSleepNone) {
+  if (tc::mbar_try(bar, parity)) return true;   // the common case, without touching the stop flag
   if (*reinterpret_cast<volatile int*>(&S.stop)) return false;
   if (tc::mbar_wait(bar, parity, kTWaitNs, sleep_ns)) return true;
   atomicExch(err, DEVERR_RING);

@@ -52,15 +52,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
 __device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-// waits in hardware (the thread is suspended, not spinning) until the phase
-// with this parity completes or about 20 us pass; true if it completed
+// true if the phase with this parity has completed; if not, the thread is
+// suspended in hardware (not spinning) until it completes or a system time
+// limit (a few microseconds on this GPU) passes.  A suspend-time hint would
+// add about 35 cycles to every call on a completed phase and is not given.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, unsigned parity) {
   unsigned ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(20000)
-      : "memory");
+  asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+               : "=r"(ok)
+               : "r"(bar), "r"(parity)
+               : "memory");
   return ok != 0;
 }
 // true once the phase with this parity has completed; false after limit_ns
