@@ -565,7 +565,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
       const uint32_t d_tmem = tmem + (uint32_t)(buf * kMaxWN);
       for (int ks = 0; ks < nk && ok; ++ks, ++ga) {
         const int as = (int)(ga % kARing);
-        if (lane == 0) ok = wait_or_stop(S, tc::smem_u32(&S.afull[as]), (ga / kARing) & 1u, g.err);
+        // INT4 / FP8: a dequantisation warp has waited for this K step's
+        // activation tile before it marked the weight tile full (below), so the
+        // weight tile's barrier covers both and this warp waits once per step
+        if (!kDq && lane == 0) ok = wait_or_stop(S, tc::smem_u32(&S.afull[as]), (ga / kARing) & 1u, g.err);
         const uint32_t a_u = tc::smem_u32(acts + (size_t)as * kATile);
         {
           const int tb = (int)(gt % (unsigned)NTL);
@@ -678,9 +681,17 @@ __global__ void __launch_bounds__(kTThreads, 1)
           }
           __syncwarp();
           if (lane == 0) {
+            // the first warp of the group also waits for the step's activation
+            // tile: the tile barrier then completes only once both operands are
+            // in place (TMA complete_tx -> this acquire -> the release of the
+            // arrive -> the MMA issuer's acquire)
+            if (wq == 0 && ok)
+              ok = wait_or_stop(S, tc::smem_u32(&S.afull[u % kARing]), (u / kARing) & 1u, g.err, kSleepShort);
             mbar_arrive(tc::smem_u32(&S.tfull[tb]));
             mbar_arrive(tc::smem_u32(&S.rempty[rs]));
           }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
         }
         if (!ok) break;
         gu += (unsigned)upi;
