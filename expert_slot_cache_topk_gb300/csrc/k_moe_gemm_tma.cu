@@ -8,9 +8,9 @@
 // expert by expert and cuts each expert's run into tiles of at most 64;
 // k_gather copies the tiles' activation rows into that order.  A work item is
 // (tile, WN weight rows), WN = 256 (128 where the shape does not divide):
-//   up:   D[128 x WN] = X . [WN/2 gate rows | WN/2 up rows of features f0 ..]^T,
+//   up:   D[64 x WN] = X . [WN/2 gate rows | WN/2 up rows of features f0 ..]^T,
 //         epilogue h = w * silu(gate) * up, stored bf16 in tile order;
-//   down: D[128 x WN] = H . [WN W2 rows]^T, epilogue: f32 rows per assignment;
+//   down: D[64 x WN] = H . [WN W2 rows]^T, epilogue: f32 rows per assignment;
 // k_combine then sums the k rows of each token in j order.
 //
 // Why weights on N: on this GPU one tcgen05.mma of kind::f16 (M = 64 or 128,
