@@ -667,6 +667,40 @@ def batched_decode(args, dev, world, src, pk) -> dict:
     return out
 
 
+def gemm_bf16_resident(args, dev, world, pk, layers: int = 4, tokens: int = 256) -> dict:
+    """The grouped GEMM on bf16 weights: OLMoE-shaped steps of 256 tokens with
+    every expert resident (no copies), so each layer step reads the distinct
+    experts' weight rows from HBM once per token tile."""
+    from expert_slot_cache_topk_gb300._abi import MoECache
+    w = synth.WORKLOADS["olmoe"].with_(layers=layers, tokens=tokens, slots=synth.WORKLOADS["olmoe"].experts)
+    c = MoECache(w.layers, w.experts, w.top_k, w.hidden, w.inter, w.wdtype, w.slots, w.tokens,
+                 copy_mode="auto", device=dev.index)
+    fill_weights(c, w)
+    run = DecodeRun(c, w, dev, warmup=args.batched_warmup, steps=args.batched_steps)
+    r = run.measure(world)
+    c.close()
+    max_sec, toks = aggregate(r["sec"], run.steps * w.tokens, world, dev)
+    tm = r["tm"]
+    gemm_s = tm["up_ms"] / 1e3
+    # weight bytes: the distinct experts of every timed layer step
+    lg = run.lg[run.warmup:]                                       # [steps, L, T, E]
+    top = np.argpartition(-lg, w.top_k - 1, axis=-1)[..., :w.top_k]
+    distinct = sum(len(np.unique(top[s, l])) for s in range(lg.shape[0]) for l in range(lg.shape[1]))
+    wbytes = distinct * synth.expert_layout(w.wdtype, w.hidden, w.inter)["total"]
+    flops = run.steps * w.layers * w.tokens * w.top_k * 2 * 3 * w.hidden * w.inter
+    gbs = wbytes / gemm_s / 1e9 if gemm_s > 0 else None
+    return {"workload": (f"bf16 grouped GEMM: {w.layers} MoE layers x {w.experts} experts (all resident), "
+                         f"top-{w.top_k}, hidden {w.hidden}, expert inter {w.inter}, {w.tokens} tokens per step"),
+            "warmup_steps": run.warmup, "steps": run.steps, "value": toks / max_sec, "unit": UNIT,
+            "ms_per_layer": 1e3 * gemm_s / (run.steps * w.layers),
+            "distinct_experts_per_layer_step": distinct / (run.steps * w.layers),
+            "roofline": {"kernel": "k_moe_gemm_tma (group + gather + up + down + combine)", "bound": "hbm",
+                         "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"] if gbs else None,
+                         "bytes": "distinct experts' weight rows per layer step, read once"},
+            "tflops": flops / gemm_s / 1e12 if gemm_s > 0 else None}
+
+
 # ---------------------------------------------------------------------------
 # prefill chunk (bypass + cold set), then decode on the same cache
 # ---------------------------------------------------------------------------
@@ -938,6 +972,7 @@ def run_ours(args, w):
         line["int4_decode"] = int4_decode(args, dev, world, src, pk)
     if not args.no_batched:
         line["batched_decode"] = batched_decode(args, dev, world, src, pk)
+        line["gemm_bf16_resident"] = gemm_bf16_resident(args, dev, world, pk)
     if not args.no_prefill:
         line["prefill"] = run_prefill(args, dev, world, src, pk)
     line["setup_s"]["int4_weights"] = src.gen_s
