@@ -94,7 +94,7 @@ struct RingShared {
 };
 
 struct RingCfg {
-  int up_pairs;           // row pairs per up item: kConsumers or kConsumers / 2
+  int up_pairs;           // row pairs per up item: 2 * kConsumers (INT4), kConsumers or kConsumers / 2
   int nstages;            // ring stages
   unsigned stage_bytes;   // bytes per stage (multiple of 128)
   int down_rows;          // output rows per down item (<= kConsumers)
@@ -573,6 +573,7 @@ __device__ __forceinline__ float swiglu_h(const RingShared& S, unsigned long lon
 // d.asg).  The stage holds [gate rows (P) | up rows (P) | gate scales (P) |
 // up scales (P)], so stage row r is gate row p0 + r for r < P, else up row
 // I + p0 + r - P.
+//   P == 2 * kConsumers (INT4): warp cw takes pairs cw and cw + kConsumers.
 //   P == kConsumers: warp cw takes pair cw, both of its rows.
 //   P == kConsumers / 2: warp cw takes stage row cw alone; the two warps of a
 //   pair meet through S.gu / S.cnt of this stage (the second one to finish
@@ -600,7 +601,23 @@ __device__ __forceinline__ void up_item(const MlpArgs& a, RingShared& S, const R
                 : reinterpret_cast<const uint16_t*>(blk + a.off_s13) + (size_t)wrow(r) * G;
   };
   auto cpyp = [&](int r) { return reinterpret_cast<uint4*>(base + (size_t)wrow(r) * rb); };
-  if (P == kConsumers) {
+  if (F == MOE_INT4_G128 && P == 2 * kConsumers) {
+    // (INT4 only) warp cw takes pairs cw and cw + kConsumers, all four rows
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    const int c2 = cw + kConsumers;
+    if (d.src != SRC_NONE) {
+      const uint4* const rows[4] = {rowp(cw), rowp(c2), rowp(P + cw), rowp(P + c2)};
+      const uint16_t* const srows[4] = {srowp(cw), srowp(c2), srowp(P + cw), srowp(P + c2)};
+      uint4* const cpys[4] = {copy ? cpyp(cw) : nullptr, copy ? cpyp(c2) : nullptr, copy ? cpyp(P + cw) : nullptr,
+                              copy ? cpyp(P + c2) : nullptr};
+      if constexpr (F == MOE_INT4_G128) rows_dot<F, 4>(rows, srows, cpys, ring, copy, C, xr, lane, v);
+    }
+    if (lane < kHRep) {
+      float* hrow = a.h + (size_t)lane * a.k * a.I + (size_t)d.asg * a.I + d.p0;
+      hrow[cw] = swiglu_h<F>(S, base, d.asg, v[0], v[2]);
+      hrow[c2] = swiglu_h<F>(S, base, d.asg, v[1], v[3]);
+    }
+  } else if (P == kConsumers) {
     float v[2] = {0.f, 0.f};
     if (d.src != SRC_NONE) {
       const uint4* const rows[2] = {rowp(cw), rowp(P + cw)};
@@ -1244,6 +1261,11 @@ bool ring_geometry(int F, int H, int I, int k, RingCfg* rc, size_t* dyn_smem) {
   // fit and a CTA's whole share of W2 can be in flight before the grid barrier
   int P = kConsumers;
   if ((size_t)2 * P * (rb1 + srb1) > 64 * 1024) P = kConsumers / 2;
+  // INT4: items of 2 * kConsumers pairs (two pairs per warp) while a stage stays
+  // within 64 KiB: a warp's rows of one item are four independent dot
+  // products, and half as many items each wait for a stage
+  if (q && (size_t)2 * (2 * kConsumers) * (rb1 + srb1) <= 64 * 1024 && I % (2 * kConsumers) == 0)
+    P = 2 * kConsumers;
   if (I % P) return false;
   size_t sb = (size_t)2 * P * (rb1 + srb1);
   int down_rows, down_group;
