@@ -94,7 +94,7 @@ struct RingShared {
 };
 
 struct RingCfg {
-  int up_pairs;           // row pairs per up item: 2 * kConsumers (INT4), kConsumers or kConsumers / 2
+  int up_pairs;           // row pairs per up item: 2 * kConsumers (INT4, FP8), kConsumers or kConsumers / 2
   int nstages;            // ring stages
   unsigned stage_bytes;   // bytes per stage (multiple of 128)
   int down_rows;          // output rows per down item (<= kConsumers)
@@ -573,7 +573,7 @@ __device__ __forceinline__ float swiglu_h(const RingShared& S, unsigned long lon
 // d.asg).  The stage holds [gate rows (P) | up rows (P) | gate scales (P) |
 // up scales (P)], so stage row r is gate row p0 + r for r < P, else up row
 // I + p0 + r - P.
-//   P == 2 * kConsumers (INT4): warp cw takes pairs cw and cw + kConsumers.
+//   P == 2 * kConsumers (INT4, FP8): warp cw takes pairs cw and cw + kConsumers.
 //   P == kConsumers: warp cw takes pair cw, both of its rows.
 //   P == kConsumers / 2: warp cw takes stage row cw alone; the two warps of a
 //   pair meet through S.gu / S.cnt of this stage (the second one to finish
@@ -601,8 +601,8 @@ __device__ __forceinline__ void up_item(const MlpArgs& a, RingShared& S, const R
                 : reinterpret_cast<const uint16_t*>(blk + a.off_s13) + (size_t)wrow(r) * G;
   };
   auto cpyp = [&](int r) { return reinterpret_cast<uint4*>(base + (size_t)wrow(r) * rb); };
-  if (F == MOE_INT4_G128 && P == 2 * kConsumers) {
-    // (INT4 only) warp cw takes pairs cw and cw + kConsumers, all four rows
+  if ((F == MOE_INT4_G128 || F == MOE_FP8_E4M3) && P == 2 * kConsumers) {
+    // (INT4, FP8) warp cw takes pairs cw and cw + kConsumers, all four rows
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     const int c2 = cw + kConsumers;
     if (d.src != SRC_NONE) {
@@ -610,7 +610,7 @@ __device__ __forceinline__ void up_item(const MlpArgs& a, RingShared& S, const R
       const uint16_t* const srows[4] = {srowp(cw), srowp(c2), srowp(P + cw), srowp(P + c2)};
       uint4* const cpys[4] = {copy ? cpyp(cw) : nullptr, copy ? cpyp(c2) : nullptr, copy ? cpyp(P + cw) : nullptr,
                               copy ? cpyp(P + c2) : nullptr};
-      if constexpr (F == MOE_INT4_G128) rows_dot<F, 4>(rows, srows, cpys, ring, copy, C, xr, lane, v);
+      if constexpr (F == MOE_INT4_G128 || F == MOE_FP8_E4M3) rows_dot<F, 4>(rows, srows, cpys, ring, copy, C, xr, lane, v);
     }
     if (lane < kHRep) {
       float* hrow = a.h + (size_t)lane * a.k * a.I + (size_t)d.asg * a.I + d.p0;
@@ -1261,10 +1261,11 @@ bool ring_geometry(int F, int H, int I, int k, RingCfg* rc, size_t* dyn_smem) {
   // fit and a CTA's whole share of W2 can be in flight before the grid barrier
   int P = kConsumers;
   if ((size_t)2 * P * (rb1 + srb1) > 64 * 1024) P = kConsumers / 2;
-  // INT4: items of 2 * kConsumers pairs (two pairs per warp) while a stage stays
+  // INT4 / FP8: items of 2 * kConsumers pairs (two pairs per warp) while a stage stays
   // within 64 KiB: a warp's rows of one item are four independent dot
   // products, and half as many items each wait for a stage
-  if (q && (size_t)2 * (2 * kConsumers) * (rb1 + srb1) <= 64 * 1024 && I % (2 * kConsumers) == 0)
+  if ((q || F == MOE_FP8_E4M3) && (size_t)2 * (2 * kConsumers) * (rb1 + srb1) <= 64 * 1024 &&
+      I % (2 * kConsumers) == 0)
     P = 2 * kConsumers;
   if (I % P) return false;
   size_t sb = (size_t)2 * P * (rb1 + srb1);
