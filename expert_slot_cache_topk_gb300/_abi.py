@@ -37,6 +37,7 @@ MOE_SLOT_POOL, MOE_SLOT_SCRATCH, MOE_SLOT_COLD = 0 << 29, 1 << 29, 2 << 29
 MOE_FWD_RESIDUAL = 1
 MOE_GEMM_NONE, MOE_GEMM_TC, MOE_GEMM_TMA = 0, 1, 2
 GEMM_KERNEL_NAME = {MOE_GEMM_NONE: "none", MOE_GEMM_TC: "tc", MOE_GEMM_TMA: "tma"}
+GEMM_KERNEL_PREF = {"auto": 0, "tc": MOE_GEMM_TC, "tma": MOE_GEMM_TMA}
 
 
 class moe_cache_config(C.Structure):
@@ -46,7 +47,8 @@ class moe_cache_config(C.Structure):
                 ("cold_mask_h", C.POINTER(C.c_uint8)), ("copy_mode", C.c_int), ("device", C.c_int),
                 ("hbm_budget_bytes", C.c_size_t), ("mlp_kernel", C.c_int),
                 ("move_interval", C.c_int), ("move_decay", C.c_float), ("move_threshold", C.c_float),
-                ("move_count_tokens", C.c_int), ("evict_policy", C.c_int), ("table_layout", C.c_int)]
+                ("move_count_tokens", C.c_int), ("evict_policy", C.c_int), ("table_layout", C.c_int),
+                ("gemm_kernel", C.c_int)]
 
 
 class moe_cache_counters(C.Structure):
@@ -190,11 +192,12 @@ class MoECache:
 
     def __init__(self, num_layers, num_experts, top_k, hidden, inter, wdtype, slots, max_tokens,
                  renormalize=False, cold_mask=None, copy_mode="uva", device=0, hbm_budget_bytes=0,
-                 mlp_kernel="auto", moves=None, policy="lru", table="split"):
+                 mlp_kernel="auto", moves=None, policy="lru", table="split", gemm_kernel="auto"):
         """moves: None (off) or a dict with interval, decay, threshold, count_tokens
         (run-time moves between the cold set and the pool; see moe_cache_config).
         policy: the eviction policy, one of EVICT_POLICY's keys.
-        table: "split" (device pool + pinned backing store) or "vmm" (one VMM table per layer)."""
+        table: "split" (device pool + pinned backing store) or "vmm" (one VMM table per layer).
+        gemm_kernel: "auto" (the TMA grouped GEMM where it runs) or "tc" (the cp.async one)."""
         self.L, self.E, self.k, self.H, self.I = num_layers, num_experts, top_k, hidden, inter
         self.wdtype, self.N, self.max_tokens = wdtype, slots, max_tokens
         cfg = moe_cache_config()
@@ -213,6 +216,7 @@ class MoECache:
         cfg.mlp_kernel = MLP_KERNEL[mlp_kernel]
         cfg.evict_policy = EVICT_POLICY[policy]
         cfg.table_layout = TABLE_LAYOUT[table]
+        cfg.gemm_kernel = GEMM_KERNEL_PREF[gemm_kernel]
         if moves:
             cfg.move_interval = int(moves.get("interval", 8))
             cfg.move_decay = float(moves.get("decay", 2.0 ** (-1.0 / 64.0)))

@@ -699,6 +699,8 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
   if (g.renormalize != 0 && g.renormalize != 1) return fail(nullptr, MOE_EINVAL, "renormalize must be 0 or 1");
   if (g.table_layout != MOE_TABLE_SPLIT && g.table_layout != MOE_TABLE_VMM)
     return fail(nullptr, MOE_EINVAL, "table_layout must be MOE_TABLE_SPLIT or MOE_TABLE_VMM");
+  if (g.gemm_kernel < 0 || g.gemm_kernel > MOE_GEMM_TMA)
+    return fail(nullptr, MOE_EINVAL, "gemm_kernel must be 0, MOE_GEMM_TC or MOE_GEMM_TMA");
   if (g.evict_policy < MOE_EVICT_LRU || g.evict_policy > MOE_EVICT_SLRU)
     return fail(nullptr, MOE_EINVAL, "evict_policy must be MOE_EVICT_LRU, _LFU, _FIFO or _SLRU");
   if (g.move_interval < 0) return fail(nullptr, MOE_EINVAL, "move_interval must be >= 0");
@@ -853,7 +855,7 @@ moe_status moe_cache_create(const moe_cache_config* cfg, moe_cache_t** out) {
     CKC(dmalloc((void**)&c->gout_d, TK * c->H * sizeof(float)));
     CKC(moe_gemm_configure(c->wd));
     c->gemm_mlp = true;
-    if (moe_gemm_tma_supported(c->wd, c->H, c->I, c->K)) {
+    if (g.gemm_kernel != MOE_GEMM_TC && moe_gemm_tma_supported(c->wd, c->H, c->I, c->K)) {
       // the TMA GEMM: activation rows gathered in tile order, tensor maps over
       // the pool (device rows of every layer), the scratch and the h rows
       const size_t rows = TK > 128 ? TK : 128;   // every activation box (<= 128 rows) inside the buffers

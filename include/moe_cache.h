@@ -198,6 +198,9 @@ typedef struct {
   int move_count_tokens; /* >= 1 */
   int evict_policy;      /* moe_evict_policy */
   int table_layout;      /* moe_table_layout */
+  int gemm_kernel;       /* steps of several tokens: 0 = automatic (MOE_GEMM_TMA where the driver
+                            and the shape allow it, else MOE_GEMM_TC); MOE_GEMM_TC = the cp.async
+                            kernel even where the TMA kernel would run; MOE_GEMM_TMA = automatic */
 } moe_cache_config;
 
 /* Cumulative per-layer counters (moe_cache_stats with layer = -1 sums layers).
@@ -251,9 +254,10 @@ typedef struct {
  *  MOE_GEMM_NONE  the per-token kernels (max_tokens 1, f32 weights, or a shape
  *                 the tensor-core kernels do not take)
  *  MOE_GEMM_TC    tcgen05, tokens on M, operands staged with cp.async
- *  MOE_GEMM_TMA   tcgen05, weight rows on M and tokens on N, operands staged by
- *                 TMA from tensor maps, warp-specialised (the default when the
- *                 CUDA driver provides tensor-map encoding) */
+ *  MOE_GEMM_TMA   tcgen05, weight rows on N (256 per instruction) and the tile's
+ *                 tokens on M = 64, operands staged by TMA from tensor maps,
+ *                 warp-specialised with dequantisation warps (the default when
+ *                 the CUDA driver provides tensor-map encoding) */
 #define MOE_GEMM_NONE 0
 #define MOE_GEMM_TC 1
 #define MOE_GEMM_TMA 2

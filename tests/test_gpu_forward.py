@@ -385,3 +385,22 @@ def test_multi_token_steps_on_the_tensor_cores(name, T, slots, over):
         ref = oracle_y(w, wt, 0, xs[s], lgs[s])
         assert_close(y_to_f64(w, ys[s]), ref, f"{name} T={T} step {s}")
         assert_close(y_to_f64(w, yp[s]), ref, f"{name} T={T} plain step {s}")
+
+
+@pytest.mark.parametrize("name,T,over", [("olmoe", 16, {}), ("int4", 24, {}), ("olmoe", 12, {"wdtype": "fp8"})])
+def test_multi_token_steps_on_the_cp_async_gemm(name, T, over):
+    """gemm_kernel="tc" keeps the cp.async grouped GEMM in use (the kernel that
+    runs where the driver provides no tensor-map encoder): every token against
+    the float64 oracle."""
+    w = W[name].with_(layers=1, tokens=T, **over)
+    steps = 3
+    lgs = synth.routing_logits(w, 0, steps)
+    xs = synth.hidden_states(w, 0, steps)
+    wt = OracleWeights(w)
+    c = make_cache(w, gemm_kernel="tc")
+    assert c.info()["gemm_kernel_name"] == "tc"
+    ys = _forward_steps(c, w, 0, xs, lgs)
+    c.check()
+    c.close()
+    for s in range(steps):
+        assert_close(y_to_f64(w, ys[s]), oracle_y(w, wt, 0, xs[s], lgs[s]), f"{name} T={T} cp.async step {s}")
